@@ -1,0 +1,621 @@
+// C ABI of the Clef JointSchemaHead forward pass: host-side validation, the
+// launch plan of one batch, the workspace layout and the launch sequence.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/clef_head.h"
+#include "common.cuh"
+#include "head_kernels.h"
+#include "kernels.h"
+
+using namespace clef;
+
+namespace {
+
+constexpr int kTile = 128;  // rows per GEMM output tile; records are padded to it in compact row space
+
+bool config_ok(const clef_config* c) {
+    if (!c) return false;
+    if (c->hidden < 64 || c->hidden > 8192 || c->hidden % 64) return false;
+    if (c->heads < 1 || c->width != 64 * c->heads || c->width > 2048) return false;
+    if (c->ffn < 64 || c->ffn % 64) return false;
+    if (c->n_route < 1 || c->n_route > 4 || c->n_joint < 0 || c->n_joint > 8) return false;
+    if (c->vocab < 1) return false;
+    return true;
+}
+
+struct WIdx {
+    int nr, nj;
+    explicit WIdx(const clef_config* c) : nr(c->n_route), nj(c->n_joint) {}
+    int route(int l, int k) const { return 6 + 16 * l + k; }
+    int mid(int k) const { return 6 + 16 * nr + k; }
+    int joint(int i, int k) const { return 6 + 16 * nr + 9 + 12 * i + k; }
+    int tail(int k) const { return 6 + 16 * nr + 9 + 12 * nj + k; }
+    int count() const { return 6 + 16 * nr + 9 + 12 * nj + 8; }
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Carve {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        size_t o = off;
+        off = align256(off + bytes);
+        return o;
+    }
+};
+
+struct PreparedLayout {
+    size_t wkv, ckv, bkv, wq0, wfield, total;
+    PreparedLayout(const clef_config* c) {
+        const size_t H = c->hidden, D = c->width, NKV = size_t(2) * c->n_route * D;
+        Carve cv;
+        wkv = cv.take(NKV * H * 2);
+        ckv = cv.take(NKV * 4);
+        bkv = cv.take(NKV * 4);
+        wq0 = cv.take(D * 3 * H * 2);
+        wfield = cv.take(D * (2 * H + D) * 2);
+        total = cv.off;
+    }
+};
+
+// Host-built plan of one batch: tables the kernels index, and sizes.
+struct Plan {
+    int B = 0, Q = 0, O = 0, R = 0, n_mtiles = 0, n_items = 0, n_chunks = 0;
+    int64_t P = 0;  // attention partial rows
+    std::vector<int32_t> blob;  // int32 tables followed by the int64 partial offsets
+    // offsets (in int32 units) of each table in the blob
+    size_t lengths, rec_row_off, rec_q_off, rec_o_off, q_rec, q_type, q_span, q_opt_off, o_rec, o_q, o_span,
+        tile_rec, tile_a_row, item_kind, item_index, chunk_rec, chunk_idx, rec_part_off;
+};
+
+int validate_schema(const clef_config* c, const clef_schema* s) {
+    if (!s || !s->lengths || !s->q_rec || !s->q_type || !s->q_span || !s->q_opt_off || !s->o_span)
+        return CLEF_ERR_INVALID_ARGUMENT;
+    if (s->B < 1 || s->Lpad < 1 || s->Q < 1 || s->O < 1) return CLEF_ERR_INVALID_ARGUMENT;
+    if (s->row_stride < c->hidden || s->row_stride % 8) return CLEF_ERR_INVALID_ARGUMENT;
+    if (int64_t(s->B) * s->Lpad >= (int64_t(1) << 31)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    for (int b = 0; b < s->B; ++b)
+        if (s->lengths[b] < 1 || s->lengths[b] > s->Lpad) return CLEF_ERR_INVALID_ARGUMENT;
+    if (s->q_opt_off[0] != 0 || s->q_opt_off[s->Q] != s->O) return CLEF_ERR_INVALID_ARGUMENT;
+    std::vector<int> per_rec(s->B, 0);
+    for (int q = 0; q < s->Q; ++q) {
+        const int b = s->q_rec[q];
+        if (b < 0 || b >= s->B) return CLEF_ERR_INVALID_ARGUMENT;
+        if (q > 0 && b < s->q_rec[q - 1]) return CLEF_ERR_INVALID_ARGUMENT;
+        ++per_rec[b];
+        const int t = s->q_type[q];
+        if (t < 0 || t > 2) return CLEF_ERR_INVALID_ARGUMENT;
+        const int st = s->q_span[2 * q], en = s->q_span[2 * q + 1];
+        if (st < 0 || st >= en || en > s->lengths[b]) return CLEF_ERR_INVALID_ARGUMENT;
+        const int n = s->q_opt_off[q + 1] - s->q_opt_off[q];
+        if (n < 1 || n > kMaxOptions) return CLEF_ERR_INVALID_ARGUMENT;
+        if (t == 0 && n != 2) return CLEF_ERR_INVALID_ARGUMENT;
+        for (int j = s->q_opt_off[q]; j < s->q_opt_off[q + 1]; ++j) {
+            const int os = s->o_span[2 * j], oe = s->o_span[2 * j + 1];
+            if (os < 0 || os >= oe || oe > s->lengths[b]) return CLEF_ERR_INVALID_ARGUMENT;
+        }
+    }
+    for (int b = 0; b < s->B; ++b) {
+        if (per_rec[b] < 1) return CLEF_ERR_INVALID_ARGUMENT;
+        if (per_rec[b] > kMaxFields) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    }
+    return CLEF_OK;
+}
+
+void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
+    p.B = s->B;
+    p.Q = s->Q;
+    p.O = s->O;
+    std::vector<int32_t>& v = p.blob;
+    v.clear();
+    auto put = [&](size_t n) {
+        size_t o = v.size();
+        v.resize(o + n, 0);
+        return o;
+    };
+    const int B = s->B, Q = s->Q, O = s->O;
+    p.lengths = put(B);
+    p.rec_row_off = put(B + 1);
+    p.rec_q_off = put(B + 1);
+    p.rec_o_off = put(B + 1);
+    p.q_rec = put(Q);
+    p.q_type = put(Q);
+    p.q_span = put(2 * size_t(Q));
+    p.q_opt_off = put(Q + 1);
+    p.o_rec = put(O);
+    p.o_q = put(O);
+    p.o_span = put(2 * size_t(O));
+    int R = 0;
+    int nch = 0;
+    for (int b = 0; b < B; ++b) {
+        v[p.lengths + b] = s->lengths[b];
+        v[p.rec_row_off + b] = R;
+        R += (s->lengths[b] + kTile - 1) / kTile * kTile;
+        nch += (s->lengths[b] + kAttnChunk - 1) / kAttnChunk;
+    }
+    v[p.rec_row_off + B] = R;
+    p.R = R;
+    p.n_mtiles = R / kTile;
+    std::vector<int> rq(B + 1, 0), ro(B + 1, 0);
+    for (int q = 0; q < Q; ++q) {
+        const int b = s->q_rec[q];
+        v[p.q_rec + q] = b;
+        v[p.q_type + q] = s->q_type[q];
+        v[p.q_span + 2 * q] = s->q_span[2 * q];
+        v[p.q_span + 2 * q + 1] = s->q_span[2 * q + 1];
+        ++rq[b + 1];
+        ro[b + 1] += s->q_opt_off[q + 1] - s->q_opt_off[q];
+        for (int j = s->q_opt_off[q]; j < s->q_opt_off[q + 1]; ++j) {
+            v[p.o_rec + j] = b;
+            v[p.o_q + j] = q;
+        }
+    }
+    for (int q = 0; q <= Q; ++q) v[p.q_opt_off + q] = s->q_opt_off[q];
+    for (int j = 0; j < 2 * O; ++j) v[p.o_span + j] = s->o_span[j];
+    for (int b = 0; b < B; ++b) {
+        rq[b + 1] += rq[b];
+        ro[b + 1] += ro[b];
+    }
+    for (int b = 0; b <= B; ++b) {
+        v[p.rec_q_off + b] = rq[b];
+        v[p.rec_o_off + b] = ro[b];
+    }
+    p.tile_rec = put(p.n_mtiles);
+    p.tile_a_row = put(p.n_mtiles);
+    {
+        int m = 0;
+        for (int b = 0; b < B; ++b) {
+            const int nt = (s->lengths[b] + kTile - 1) / kTile;
+            for (int k = 0; k < nt; ++k, ++m) {
+                v[p.tile_rec + m] = b;
+                v[p.tile_a_row + m] = b * s->Lpad + k * kTile;
+            }
+        }
+    }
+    p.n_items = Q + O + B;
+    p.item_kind = put(p.n_items);
+    p.item_index = put(p.n_items);
+    {
+        int i = 0;
+        for (int q = 0; q < Q; ++q, ++i) { v[p.item_kind + i] = 0; v[p.item_index + i] = q; }
+        for (int j = 0; j < O; ++j, ++i) { v[p.item_kind + i] = 1; v[p.item_index + i] = j; }
+        for (int b = 0; b < B; ++b, ++i) { v[p.item_kind + i] = 2; v[p.item_index + i] = b; }
+    }
+    p.n_chunks = nch;
+    p.chunk_rec = put(nch);
+    p.chunk_idx = put(nch);
+    {
+        int i = 0;
+        for (int b = 0; b < B; ++b) {
+            const int n = (s->lengths[b] + kAttnChunk - 1) / kAttnChunk;
+            for (int k = 0; k < n; ++k, ++i) { v[p.chunk_rec + i] = b; v[p.chunk_idx + i] = k; }
+        }
+    }
+    if (v.size() & 1) put(1);  // 8-byte alignment of the int64 table
+    p.rec_part_off = put(2 * size_t(B));
+    int64_t P = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t off = P;
+        std::memcpy(&v[p.rec_part_off + 2 * b], &off, 8);
+        const int n = (s->lengths[b] + kAttnChunk - 1) / kAttnChunk;
+        P += int64_t(n) * c->heads * (ro[b + 1] - ro[b]);
+    }
+    p.P = P;
+}
+
+struct WsLayout {
+    size_t flags, plan, mu, rstd, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf, q_buf, attn_buf, hid_buf,
+        o_hat, f_res, f_hat, z, pm, pl, pacc, total;
+    WsLayout(const clef_config* c, const Plan& p) {
+        const size_t H = c->hidden, D = c->width, F = c->ffn, NKV = size_t(2) * c->n_route * D;
+        const size_t B = p.B, Q = p.Q, O = p.O, R = p.R, MQO = std::max(Q, O);
+        Carve cv;
+        flags = cv.take(256);
+        plan = cv.take(p.blob.size() * 4);
+        mu = cv.take(R * 4);
+        rstd = cv.take(R * 4);
+        kv = cv.take(R * NKV * 2);
+        a_query = cv.take(O * 3 * H * 2);
+        a_field = cv.take(Q * (2 * H + D) * 2);
+        u32 = cv.take(Q * H * 4);
+        x32 = cv.take(O * H * 4);
+        g32 = cv.take(B * H * 4);
+        o_res = cv.take(O * D * 4);
+        ln_buf = cv.take(MQO * D * 2);
+        q_buf = cv.take(std::max(O * D, Q * 3 * D) * 2);
+        attn_buf = cv.take(MQO * D * 2);
+        hid_buf = cv.take(MQO * std::max(F, D) * 2);
+        o_hat = cv.take(O * D * 4);
+        f_res = cv.take(Q * D * 4);
+        f_hat = cv.take(Q * D * 4);
+        z = cv.take(O * 4 * D * 2);
+        pm = cv.take(size_t(p.P) * 4);
+        pl = cv.take(size_t(p.P) * 4);
+        pacc = cv.take(size_t(p.P) * 64 * 4);
+        total = cv.off;
+    }
+};
+
+// Last plan uploaded into each workspace: an identical schema skips the upload.
+std::mutex g_plan_mu;
+std::unordered_map<const void*, std::vector<int32_t>> g_uploaded;
+
+// The status word of a workspace seen for the first time is cleared here; after
+// that it accumulates device-side flags until clef_device_status reads it.
+int upload_plan(const Plan& p, void* workspace, void* dst, cudaStream_t st) {
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        auto it = g_uploaded.find(dst);
+        if (it != g_uploaded.end() && it->second == p.blob) return CLEF_OK;
+        if (it == g_uploaded.end() && cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return CLEF_ERR_CUDA;
+    }
+    if (cudaMemcpyAsync(dst, p.blob.data(), p.blob.size() * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return CLEF_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    g_uploaded[dst] = p.blob;
+    return CLEF_OK;
+}
+
+#define CK(x)                                   \
+    do {                                        \
+        if ((x) != cudaSuccess) return CLEF_ERR_CUDA; \
+    } while (0)
+
+inline const uint16_t* W(const void* const* w, int i) { return static_cast<const uint16_t*>(w[i]); }
+
+inline cudaError_t mark(const clef_debug_outputs* d, int slot, cudaStream_t st) {
+    if (!d || !d->events[slot]) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(d->events[slot]), st);
+}
+
+// Dense GEMM helper: A [M][K] (lda), weight [N][K].
+cudaError_t dense(const uint16_t* A, int64_t lda, int M, const uint16_t* Bw, int N, int K, const GemmEpilogue& e,
+                  int* flags, cudaStream_t st) {
+    GemmProblem g;
+    g.A = A;
+    g.lda = lda;
+    g.a_rows = M;
+    g.B = Bw;
+    g.ldb = K;
+    g.N = N;
+    g.K = K;
+    g.n_mtiles = (M + kTile - 1) / kTile;
+    GemmEpilogue ee = e;
+    ee.M = M;
+    return launch_gemm(g, ee, flags, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* clef_status_string(int s) {
+    switch (s) {
+        case CLEF_OK: return "ok";
+        case CLEF_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case CLEF_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case CLEF_ERR_UNSUPPORTED_CONFIG: return "unsupported configuration";
+        case CLEF_ERR_CUDA: return "CUDA error";
+        case CLEF_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+        case CLEF_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int clef_weight_count(const clef_config* cfg) {
+    if (!config_ok(cfg)) return -1;
+    return WIdx(cfg).count();
+}
+
+int clef_prepared_size(const clef_config* cfg, size_t* bytes) {
+    if (!bytes) return CLEF_ERR_INVALID_ARGUMENT;
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    *bytes = PreparedLayout(cfg).total;
+    return CLEF_OK;
+}
+
+int clef_prepare_weights(const clef_config* cfg, const void* const* weights, void* prepared, size_t prepared_bytes,
+                         void* stream) {
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (!weights || !prepared || (reinterpret_cast<uintptr_t>(prepared) & 255)) return CLEF_ERR_INVALID_ARGUMENT;
+    const WIdx wi(cfg);
+    for (int i = 0; i < wi.count(); ++i)
+        if (!weights[i] || (reinterpret_cast<uintptr_t>(weights[i]) & 15)) return CLEF_ERR_INVALID_ARGUMENT;
+    const PreparedLayout L(cfg);
+    if (prepared_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(prepared);
+    const int H = cfg->hidden, D = cfg->width;
+    FoldArgs f;
+    f.H = H;
+    f.D = D;
+    for (int l = 0; l < cfg->n_route; ++l) {
+        f.w[2 * l] = W(weights, wi.route(l, 4));
+        f.bias[2 * l] = W(weights, wi.route(l, 5));
+        f.w[2 * l + 1] = W(weights, wi.route(l, 6));
+        f.bias[2 * l + 1] = W(weights, wi.route(l, 7));
+    }
+    f.gamma = W(weights, 0);
+    f.beta = W(weights, 1);
+    f.out_w = reinterpret_cast<uint16_t*>(base + L.wkv);
+    f.out_c = reinterpret_cast<float*>(base + L.ckv);
+    f.out_b = reinterpret_cast<float*>(base + L.bkv);
+    CK(launch_fold_kv(f, 2 * cfg->n_route * D, st));
+    uint16_t* wq0 = reinterpret_cast<uint16_t*>(base + L.wq0);
+    CK(launch_copy_cols(wq0, 3 * H, 0, W(weights, 2), H, D, H, st));
+    CK(launch_copy_cols(wq0, 3 * H, H, W(weights, 3), H, D, H, st));
+    CK(launch_copy_cols(wq0, 3 * H, 2 * H, W(weights, 4), H, D, H, st));
+    uint16_t* wf = reinterpret_cast<uint16_t*>(base + L.wfield);
+    const int ldf = 2 * H + D;
+    CK(launch_copy_cols(wf, ldf, 0, W(weights, wi.mid(4)), H, D, H, st));
+    CK(launch_copy_cols(wf, ldf, H, W(weights, wi.mid(6)), H, D, H, st));
+    CK(launch_copy_cols(wf, ldf, 2 * H, W(weights, wi.mid(5)), D, D, D, st));
+    return CLEF_OK;
+}
+
+int clef_workspace_size(const clef_config* cfg, const clef_schema* schema, size_t* bytes) {
+    if (!bytes) return CLEF_ERR_INVALID_ARGUMENT;
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    const int v = validate_schema(cfg, schema);
+    if (v != CLEF_OK) return v;
+    Plan p;
+    build_plan(cfg, schema, p);
+    *bytes = WsLayout(cfg, p).total;
+    return CLEF_OK;
+}
+
+int clef_head_forward(const clef_config* cfg, const void* const* weights, const void* prepared,
+                      const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
+                      const uint16_t* lexical, float* logits, float* probs, float* q_value, float* q_conf,
+                      int32_t* q_argmax, void* workspace, size_t workspace_bytes, const clef_debug_outputs* debug,
+                      void* stream) {
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (!weights || !prepared || !hidden || !token_ids || !lexical || !logits || !probs || !q_value || !q_conf ||
+        !q_argmax || !workspace)
+        return CLEF_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(hidden) & 15) || (reinterpret_cast<uintptr_t>(lexical) & 15) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(prepared) & 255))
+        return CLEF_ERR_INVALID_ARGUMENT;
+    const WIdx wi(cfg);
+    for (int i = 0; i < wi.count(); ++i)
+        if (!weights[i] || (reinterpret_cast<uintptr_t>(weights[i]) & 15)) return CLEF_ERR_INVALID_ARGUMENT;
+    const int v = validate_schema(cfg, schema);
+    if (v != CLEF_OK) return v;
+    Plan p;
+    build_plan(cfg, schema, p);
+    const WsLayout L(cfg, p);
+    if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* pw = static_cast<const uint8_t*>(prepared);
+    const PreparedLayout PL(cfg);
+    int* flags = reinterpret_cast<int*>(ws + L.flags);
+    const int32_t* plan = reinterpret_cast<const int32_t*>(ws + L.plan);
+    const int H = cfg->hidden, D = cfg->width, F = cfg->ffn, NKV = 2 * cfg->n_route * D;
+    const int B = p.B, Q = p.Q, O = p.O;
+
+    {
+        const int u = upload_plan(p, ws, ws + L.plan, st);
+        if (u != CLEF_OK) return u;
+    }
+    auto T = [&](size_t off) { return plan + off; };
+    float* mu = reinterpret_cast<float*>(ws + L.mu);
+    float* rstd = reinterpret_cast<float*>(ws + L.rstd);
+    uint16_t* kv = reinterpret_cast<uint16_t*>(ws + L.kv);
+    uint16_t* a_query = reinterpret_cast<uint16_t*>(ws + L.a_query);
+    uint16_t* a_field = reinterpret_cast<uint16_t*>(ws + L.a_field);
+    float* u32 = reinterpret_cast<float*>(ws + L.u32);
+    float* x32 = reinterpret_cast<float*>(ws + L.x32);
+    float* g32 = reinterpret_cast<float*>(ws + L.g32);
+    float* o_res = reinterpret_cast<float*>(ws + L.o_res);
+    uint16_t* ln_buf = reinterpret_cast<uint16_t*>(ws + L.ln_buf);
+    uint16_t* q_buf = reinterpret_cast<uint16_t*>(ws + L.q_buf);
+    uint16_t* attn_buf = reinterpret_cast<uint16_t*>(ws + L.attn_buf);
+    uint16_t* hid_buf = reinterpret_cast<uint16_t*>(ws + L.hid_buf);
+    float* o_hat = reinterpret_cast<float*>(ws + L.o_hat);
+    float* f_res = reinterpret_cast<float*>(ws + L.f_res);
+    float* f_hat = reinterpret_cast<float*>(ws + L.f_hat);
+    uint16_t* z = reinterpret_cast<uint16_t*>(ws + L.z);
+    const int ld_field = 2 * H + D;
+
+    // 1. memory row statistics (the memory LayerNorm is applied through them)
+    CK(mark(debug, 6, st));
+    CK(launch_row_stats(hidden, schema->row_stride, schema->Lpad, H, T(p.tile_rec), T(p.rec_row_off), T(p.lengths),
+                        p.R, mu, rstd, st));
+    CK(mark(debug, 7, st));
+    // 2. span pooling
+    SpanPoolArgs sp{};
+    sp.hidden = hidden; sp.row_stride = schema->row_stride; sp.Lpad = schema->Lpad; sp.H = H; sp.vocab = cfg->vocab;
+    sp.token_ids = token_ids; sp.lexical = lexical; sp.mu = mu; sp.rstd = rstd;
+    sp.ln_w = W(weights, 0); sp.ln_b = W(weights, 1);
+    sp.item_kind = T(p.item_kind); sp.item_index = T(p.item_index);
+    sp.lengths = T(p.lengths); sp.rec_row_off = T(p.rec_row_off); sp.rec_q_off = T(p.rec_q_off);
+    sp.q_rec = T(p.q_rec); sp.q_span = T(p.q_span); sp.q_opt_off = T(p.q_opt_off);
+    sp.o_rec = T(p.o_rec); sp.o_span = T(p.o_span);
+    sp.a_query = a_query; sp.ld_query = 3 * H; sp.a_field = a_field; sp.ld_field = ld_field;
+    sp.u32 = u32; sp.x32 = x32; sp.g32 = g32;
+    sp.dbg_c = debug ? debug->pooled_c : nullptr;
+    sp.flags = flags;
+    CK(mark(debug, 4, st));
+    CK(launch_span_pool(sp, p.n_items, false, st));
+    CK(mark(debug, 5, st));
+    // 3. option queries: o = [c | x | u] [W_ctx | W_lex | W_qst]^T + b
+    {
+        GemmEpilogue e;
+        e.kind = EPI_F32; e.bias_bf16 = W(weights, 5); e.out = o_res; e.ldo = D;
+        CK(dense(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, e, flags, st));
+    }
+    // 4. memory K/V of every routing layer (LayerNorm folded), real rows only
+    {
+        GemmProblem g;
+        g.A = hidden; g.lda = schema->row_stride; g.a_rows = int64_t(B) * schema->Lpad;
+        g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
+        g.N = NKV; g.K = H; g.n_mtiles = p.n_mtiles; g.a_row_of_mtile = T(p.tile_a_row);
+        GemmEpilogue e;
+        e.kind = EPI_KV_LNFOLD; e.row_mu = mu; e.row_rstd = rstd;
+        e.col_c = reinterpret_cast<const float*>(pw + PL.ckv);
+        e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
+        e.out = kv; e.ldo = NKV; e.M = p.R;
+        CK(mark(debug, 0, st));
+        CK(launch_gemm(g, e, flags, st));
+        CK(mark(debug, 1, st));
+    }
+    // 5. evidence routing layers
+    RouteAttnArgs ra{};
+    ra.q = q_buf; ra.ldq = D; ra.kv = kv; ra.ldkv = NKV; ra.heads = cfg->heads;
+    ra.scale_log2 = 1.4426950408889634f / 8.0f;
+    ra.chunk_rec = T(p.chunk_rec); ra.chunk_idx = T(p.chunk_idx); ra.lengths = T(p.lengths);
+    ra.rec_row_off = T(p.rec_row_off); ra.rec_o_off = T(p.rec_o_off);
+    ra.rec_part_off = reinterpret_cast<const int64_t*>(T(p.rec_part_off)); ra.o_rec = T(p.o_rec);
+    ra.pm = reinterpret_cast<float*>(ws + L.pm); ra.pl = reinterpret_cast<float*>(ws + L.pl);
+    ra.pacc = reinterpret_cast<float*>(ws + L.pacc); ra.out = attn_buf; ra.ldo = D;
+    for (int l = 0; l < cfg->n_route; ++l) {
+        CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 0)), W(weights, wi.route(l, 1)), ln_buf, nullptr, st));
+        GemmEpilogue eq;
+        eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.route(l, 3)); eq.out = q_buf; eq.ldo = D;
+        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 2)), D, D, eq, flags, st));
+        ra.k_col = 2 * l * D;
+        ra.v_col = (2 * l + 1) * D;
+        if (l == 0) CK(mark(debug, 2, st));
+        CK(launch_route_attn_partial(ra, p.n_chunks, st));
+        if (l == 0) CK(mark(debug, 3, st));
+        CK(launch_route_attn_merge(ra, O, st));
+        GemmEpilogue eo;
+        eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.route(l, 9)); eo.out = o_res; eo.ldo = D;
+        CK(dense(attn_buf, D, O, W(weights, wi.route(l, 8)), D, D, eo, flags, st));
+        CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 10)), W(weights, wi.route(l, 11)), ln_buf, nullptr,
+                             st));
+        GemmEpilogue e1;
+        e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.route(l, 13)); e1.out = hid_buf; e1.ldo = F;
+        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 12)), F, D, e1, flags, st));
+        GemmEpilogue e2;
+        e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.route(l, 15)); e2.out = o_res; e2.ldo = D;
+        CK(dense(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, e2, flags, st));
+    }
+    CK(launch_layer_norm(o_res, O, D, W(weights, wi.mid(0)), W(weights, wi.mid(1)), nullptr, o_hat, st));
+    // 6. fields: [u | g | summary] [W_fu | W_fg | W_fs]^T + b + type embedding
+    CK(launch_field_pool(o_hat, D, T(p.q_opt_off), Q, W(weights, wi.mid(2)), W(weights, wi.mid(3)), a_field, ld_field,
+                         2 * H, st));
+    {
+        GemmEpilogue e;
+        e.kind = EPI_F32; e.bias_bf16 = W(weights, wi.mid(7)); e.row_table = W(weights, wi.mid(8));
+        e.row_idx = T(p.q_type); e.ld_table = D; e.out = f_res; e.ldo = D;
+        CK(dense(a_field, ld_field, Q, reinterpret_cast<const uint16_t*>(pw + PL.wfield), D, ld_field, e, flags, st));
+    }
+    // 7. joint layers over each record's fields
+    for (int i = 0; i < cfg->n_joint; ++i) {
+        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 0)), W(weights, wi.joint(i, 1)), ln_buf, nullptr, st));
+        GemmEpilogue eq;
+        eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.joint(i, 3)); eq.out = q_buf; eq.ldo = 3 * D;
+        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 2)), 3 * D, D, eq, flags, st));
+        CK(launch_field_attn(q_buf, D, cfg->heads, T(p.rec_q_off), B, 0.125f, attn_buf, st));
+        GemmEpilogue eo;
+        eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.joint(i, 5)); eo.out = f_res; eo.ldo = D;
+        CK(dense(attn_buf, D, Q, W(weights, wi.joint(i, 4)), D, D, eo, flags, st));
+        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 6)), W(weights, wi.joint(i, 7)), ln_buf, nullptr, st));
+        GemmEpilogue e1;
+        e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.joint(i, 9)); e1.out = hid_buf; e1.ldo = F;
+        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 8)), F, D, e1, flags, st));
+        GemmEpilogue e2;
+        e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.joint(i, 11)); e2.out = f_res; e2.ldo = D;
+        CK(dense(hid_buf, F, Q, W(weights, wi.joint(i, 10)), D, F, e2, flags, st));
+    }
+    CK(launch_layer_norm(f_res, Q, D, W(weights, wi.tail(0)), W(weights, wi.tail(1)), nullptr, f_hat, st));
+    // 8. scorer MLP hidden layer, then scores, softmax and answers
+    CK(launch_build_z(f_hat, o_hat, T(p.o_q), O, D, z, st));
+    {
+        GemmEpilogue e;
+        e.kind = EPI_BF16; e.gelu = 1; e.bias_bf16 = W(weights, wi.tail(5)); e.out = hid_buf; e.ldo = D;
+        CK(dense(z, 4 * D, O, W(weights, wi.tail(4)), D, 4 * D, e, flags, st));
+    }
+    ScoreArgs sc{};
+    sc.H = H; sc.D = D; sc.q_rec = T(p.q_rec); sc.q_type = T(p.q_type); sc.q_opt_off = T(p.q_opt_off);
+    sc.u32 = u32; sc.g32 = g32; sc.x32 = x32; sc.f_hat = f_hat; sc.o_hat = o_hat; sc.mlp_hidden = hid_buf;
+    sc.w2 = W(weights, wi.tail(6)); sc.b2 = W(weights, wi.tail(7)); sc.gate = W(weights, wi.tail(2));
+    sc.joint_scale = W(weights, wi.tail(3));
+    sc.logits = logits; sc.probs = probs; sc.q_value = q_value; sc.q_conf = q_conf; sc.q_argmax = q_argmax;
+    CK(launch_score_softmax(sc, Q, st));
+    if (debug) {
+        if (debug->pooled_u) CK(cudaMemcpyAsync(debug->pooled_u, u32, size_t(Q) * H * 4, cudaMemcpyDeviceToDevice, st));
+        if (debug->pooled_x) CK(cudaMemcpyAsync(debug->pooled_x, x32, size_t(O) * H * 4, cudaMemcpyDeviceToDevice, st));
+        if (debug->global_g) CK(cudaMemcpyAsync(debug->global_g, g32, size_t(B) * H * 4, cudaMemcpyDeviceToDevice, st));
+        if (debug->option_final)
+            CK(cudaMemcpyAsync(debug->option_final, o_hat, size_t(O) * D * 4, cudaMemcpyDeviceToDevice, st));
+        if (debug->field_final)
+            CK(cudaMemcpyAsync(debug->field_final, f_hat, size_t(Q) * D * 4, cudaMemcpyDeviceToDevice, st));
+    }
+    return CLEF_OK;
+}
+
+int clef_device_status(void* workspace, void* stream) {
+    if (!workspace) return CLEF_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    CK(cudaMemcpyAsync(&h, workspace, 4, cudaMemcpyDeviceToHost, st));
+    CK(cudaStreamSynchronize(st));
+    if (h != 0) CK(cudaMemsetAsync(workspace, 0, 4, st));
+    if (h & kFlagTimeout) return CLEF_ERR_DEVICE_TIMEOUT;
+    if (h & kFlagBounds) return CLEF_ERR_DEVICE_BOUNDS;
+    return CLEF_OK;
+}
+
+int clef_span_sums(const clef_config* cfg, const clef_schema* schema, const uint16_t* hidden,
+                   const int32_t* token_ids, const uint16_t* lexical, float* q_sum, float* o_sum, float* x_sum,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (!hidden || !token_ids || !lexical || !q_sum || !o_sum || !x_sum || !workspace) return CLEF_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(hidden) & 15) || (reinterpret_cast<uintptr_t>(lexical) & 15) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(q_sum) & 15) ||
+        (reinterpret_cast<uintptr_t>(o_sum) & 15) || (reinterpret_cast<uintptr_t>(x_sum) & 15))
+        return CLEF_ERR_INVALID_ARGUMENT;
+    const int v = validate_schema(cfg, schema);
+    if (v != CLEF_OK) return v;
+    Plan p;
+    build_plan(cfg, schema, p);
+    const WsLayout L(cfg, p);
+    if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int u = upload_plan(p, ws, ws + L.plan, st);
+    if (u != CLEF_OK) return u;
+    const int32_t* plan = reinterpret_cast<const int32_t*>(ws + L.plan);
+    SpanPoolArgs sp{};
+    sp.hidden = hidden; sp.row_stride = schema->row_stride; sp.Lpad = schema->Lpad; sp.H = cfg->hidden;
+    sp.vocab = cfg->vocab; sp.token_ids = token_ids; sp.lexical = lexical;
+    sp.item_kind = plan + p.item_kind; sp.item_index = plan + p.item_index;
+    sp.lengths = plan + p.lengths; sp.rec_row_off = plan + p.rec_row_off; sp.rec_q_off = plan + p.rec_q_off;
+    sp.q_rec = plan + p.q_rec; sp.q_span = plan + p.q_span; sp.q_opt_off = plan + p.q_opt_off;
+    sp.o_rec = plan + p.o_rec; sp.o_span = plan + p.o_span;
+    sp.q_sum = q_sum; sp.o_sum = o_sum; sp.x_sum = x_sum;
+    sp.flags = reinterpret_cast<int*>(ws + L.flags);
+    CK(launch_span_pool(sp, p.n_items, true, st));
+    return CLEF_OK;
+}
+
+uint64_t clef_kernel_launches(void) { return g_kernel_launches.load(); }
+
+int clef_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, const float* bias, float* C,
+                   int64_t ldc, int32_t M, int32_t N, int32_t K, int32_t* flags, void* stream) {
+    if (!A || !B || !C || !flags) return CLEF_ERR_INVALID_ARGUMENT;
+    if (M < 1 || N < 1 || K < 1 || K % 64 || N % 64 || lda % 8 || ldb % 8 || lda < K || ldb < K || ldc < N ||
+        ldc % 4)
+        return CLEF_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) ||
+        (reinterpret_cast<uintptr_t>(C) & 15))
+        return CLEF_ERR_INVALID_ARGUMENT;
+    GemmProblem g;
+    g.A = A; g.lda = lda; g.a_rows = M; g.B = B; g.ldb = ldb; g.N = N; g.K = K;
+    g.n_mtiles = (M + kTile - 1) / kTile;
+    GemmEpilogue e;
+    e.kind = EPI_F32; e.bias_f32 = bias; e.out = C; e.ldo = ldc; e.M = M;
+    CK(launch_gemm(g, e, flags, static_cast<cudaStream_t>(stream)));
+    return CLEF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,342 @@
+// Dense bf16 contraction on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA, used for every projection of the head:
+//   - the memory K/V projection of both routing layers in one N = 4 * width GEMM,
+//     with the memory LayerNorm folded into the epilogue ("clef-4bit JointSchemaHead
+//     walkthrough" section 3 step 2: options attend the whole memory);
+//   - the option-query, routing, field, joint-layer and scorer projections.
+//
+// Design: persistent CTAs (one per SM) walk 128 x BN output tiles.  Warp 0 is the
+// TMA producer, warp 1 owns TMEM and issues tcgen05.mma (one thread), warps 2..5
+// drain the fp32 accumulators from TMEM and run the epilogue.  Two TMEM
+// accumulators let the epilogue of one tile overlap the mainloop of the next.
+// Operand tiles are 64-element K slices with the 128-byte swizzle.  Tiles are
+// visited N-fastest so that CTAs working at the same time share A tiles in L2.
+// Every mbarrier wait is bounded: on a timeout the CTA sets the timeout flag,
+// waits (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace clef {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+
+struct GemmArgs {
+    int n_mtiles, n_ntiles, kblocks;
+    const int32_t* a_row_of_mtile;
+    GemmEpilogue epi;
+    int* dev_flags;
+};
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+};
+
+template <int BN>
+__device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int n0, const uint32_t (&r)[16]) {
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+    if (e.kind == EPI_KV_LNFOLD) {
+        const float mu = e.row_mu[m], rs = e.row_rstd[m];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = rs * (v[j] - mu * e.col_c[n0 + j]) + e.bias_f32[n0 + j];
+    } else {
+        if (e.bias_bf16) {
+            const uint4* bp = reinterpret_cast<const uint4*>(e.bias_bf16 + n0);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint4 w = bp[q];
+                v[q * 8 + 0] += bf16_lo(w.x); v[q * 8 + 1] += bf16_hi(w.x);
+                v[q * 8 + 2] += bf16_lo(w.y); v[q * 8 + 3] += bf16_hi(w.y);
+                v[q * 8 + 4] += bf16_lo(w.z); v[q * 8 + 5] += bf16_hi(w.z);
+                v[q * 8 + 6] += bf16_lo(w.w); v[q * 8 + 7] += bf16_hi(w.w);
+            }
+        } else if (e.bias_f32) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += e.bias_f32[n0 + j];
+        }
+        if (e.row_table) {
+            const uint16_t* t = e.row_table + int64_t(e.row_idx[m]) * e.ld_table;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += bf16_to_float(t[n0 + j]);
+        }
+        if (e.gelu) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = gelu_exact(v[j]);
+        }
+    }
+    if (e.kind == EPI_F32 || e.kind == EPI_F32_RESID) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(e.out) + int64_t(m) * e.ldo + n0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float4 w = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            if (e.kind == EPI_F32_RESID) {
+                float4 old = o[q];
+                w.x += old.x; w.y += old.y; w.z += old.z; w.w += old.w;
+            }
+            o[q] = w;
+        }
+    } else {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.out) + int64_t(m) * e.ldo + n0);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint4 w;
+            w.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+            w.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+            w.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+            w.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+            o[q] = w;
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+    using C = GemmCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4 * 32);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_tiles = args.n_mtiles * args.n_ntiles;
+    const int kblocks = args.kblocks;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed[C::STAGES];
+            for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const int mt = tile / args.n_ntiles, nt = tile % args.n_ntiles;
+                const int a_row = args.a_row_of_mtile ? args.a_row_of_mtile[mt] : mt * BM;
+                const int b_row = nt * BN;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.dev_flags)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
+                    tma_load_2d(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, &full[stage]);
+                    tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
+                    ++armed[stage];
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {  // let every copy this thread started land before the CTA exits
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (armed[s] != 0) mbar_wait_bounded(&full[s], (armed[s] - 1) & 1u, nullptr, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t use = uint32_t(local >> 1);
+                if (!mbar_wait_bounded(&tempty[acc], (use & 1u) ^ 1u, abort_flag, args.dev_flags)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.dev_flags)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
+                                    (kb | k) != 0);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit(&tfull[acc]);
+            }
+            // every MMA this thread issued completes before TMEM is released
+            tc_commit(drain);
+            mbar_wait_bounded(drain, 0, nullptr, args.dev_flags);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;  // TMEM lanes this warp may read
+        const int r_in_tile = quarter * 32 + lane;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t use = uint32_t(local >> 1);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(&tfull[acc], use & 1u, abort_flag, args.dev_flags) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int mt = tile / args.n_ntiles, nt = tile % args.n_ntiles;
+            const int m = mt * BM + r_in_tile;
+            const bool store = m < args.epi.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 16; ++c) {
+                uint32_t r[16];
+                tmem_ld16(tmem_base + uint32_t(acc * BN + c * 16) + (uint32_t(quarter * 32) << 16), r);
+                tmem_ld_wait();
+                if (store) epilogue_chunk<BN>(args.epi, m, nt * BN + c * 16, r);
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
+              uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_elems * 2};
+    cuuint32_t box[2] = {uint32_t(BK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s) {
+    using C = GemmCfg<BN>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, p.A, uint64_t(p.K), uint64_t(p.a_rows), uint64_t(p.lda), BM)) return cudaErrorInvalidValue;
+    if (!make_map(&tb, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN)) return cudaErrorInvalidValue;
+    GemmArgs a;
+    a.n_mtiles = p.n_mtiles;
+    a.n_ntiles = p.N / BN;
+    a.kblocks = p.K / BK;
+    a.a_row_of_mtile = p.a_row_of_mtile;
+    a.epi = e;
+    a.dev_flags = flags;
+    const int tiles = a.n_mtiles * a.n_ntiles;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, s>>>(ta, tb, a);
+    return counted(cudaGetLastError());
+}
+
+}  // namespace
+
+std::atomic<uint64_t> g_kernel_launches{0};
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_flags, cudaStream_t s, int force_bn) {
+    if (p.n_mtiles <= 0 || p.N <= 0) return cudaSuccess;
+    if (p.K % BK != 0 || p.N % 64 != 0 || p.lda % 8 != 0 || p.ldb % 8 != 0) return cudaErrorInvalidValue;
+    int bn = force_bn;
+    if (bn == 0) {
+        const int sms = num_sms();
+        bn = 64;
+        if (p.N % 256 == 0 && p.n_mtiles * (p.N / 256) >= sms) bn = 256;
+        else if (p.N % 128 == 0 && p.n_mtiles * (p.N / 128) >= sms) bn = 128;
+    }
+    if (p.N % bn != 0) return cudaErrorInvalidValue;
+    switch (bn) {
+        case 256: return launch_bn<256>(p, e, dev_flags, s);
+        case 128: return launch_bn<128>(p, e, dev_flags, s);
+        default: return launch_bn<64>(p, e, dev_flags, s);
+    }
+}
+
+}  // namespace clef

@@ -1,0 +1,741 @@
+// The head's non-GEMM kernels: memory row statistics, span pooling, LayerNorm of
+// the option / field streams, split-L routing attention and its merge, field
+// aggregation, field self-attention, scorer input assembly, scoring with the
+// per-question softmax, and the weight-preparation kernels.
+#include "common.cuh"
+#include "head_kernels.h"
+#include "kernels.h"
+
+namespace clef {
+
+// =====================================================================
+// Memory row statistics: mean and 1/sqrt(var + eps) of every real hidden row,
+// indexed by compact row (record rows padded up to a 128-row boundary).  The
+// memory LayerNorm ("clef-flash-CoreAI metadata.json" decision.head.reads) is
+// applied through these statistics by the K/V projection epilogue and by pooling.
+// Rows in a record's round-up slack get mu = rstd = 0.
+// =====================================================================
+__global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restrict__ hidden, int64_t row_stride,
+                                                       int Lpad, int H, const int32_t* __restrict__ tile_rec,
+                                                       const int32_t* __restrict__ rec_row_off,
+                                                       const int32_t* __restrict__ lengths, int R,
+                                                       float* __restrict__ mu, float* __restrict__ rstd) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= R) return;
+    const int b = tile_rec[r >> 7];
+    const int t = r - rec_row_off[b];
+    if (t >= lengths[b]) {
+        if (lane == 0) { mu[r] = 0.f; rstd[r] = 0.f; }
+        return;
+    }
+    const uint4* row = reinterpret_cast<const uint4*>(hidden + (int64_t(b) * Lpad + t) * row_stride);
+    const int n8 = H >> 3;
+    float s = 0.f;
+#pragma unroll 4
+    for (int i = lane; i < n8; i += 32) {
+        uint4 w = __ldg(row + i);
+        s += bf16_lo(w.x) + bf16_hi(w.x) + bf16_lo(w.y) + bf16_hi(w.y) + bf16_lo(w.z) + bf16_hi(w.z) +
+             bf16_lo(w.w) + bf16_hi(w.w);
+    }
+    const float m = warp_sum(s) / float(H);
+    float q = 0.f;
+#pragma unroll 4
+    for (int i = lane; i < n8; i += 32) {
+        uint4 w = __ldg(row + i);
+        float d;
+        d = bf16_lo(w.x) - m; q += d * d; d = bf16_hi(w.x) - m; q += d * d;
+        d = bf16_lo(w.y) - m; q += d * d; d = bf16_hi(w.y) - m; q += d * d;
+        d = bf16_lo(w.z) - m; q += d * d; d = bf16_hi(w.z) - m; q += d * d;
+        d = bf16_lo(w.w) - m; q += d * d; d = bf16_hi(w.w) - m; q += d * d;
+    }
+    const float var = warp_sum(q) / float(H);
+    if (lane == 0) {
+        mu[r] = m;
+        rstd[r] = rsqrtf(var + 1e-5f);
+    }
+}
+
+// =====================================================================
+// Span pooling ("clef-4bit JointSchemaHead walkthrough" section 3 step 1,
+// "clef-flash-CoreAI metadata.json" decision.spans / head.reads / head.lexical).
+// One CTA per work item:
+//   kind 0, question q:  u_q = mean over the instruction span of LN(h_t)
+//   kind 1, option j:    c_j = mean over its span of LN(h_t);  x_j = mean of lexical rows of its ids
+//   kind 2, record b:    g_b = LN(h_{L_b - 1})
+// LN(h_t) = (h_t - mu_t) * rstd_t * gamma + beta; the mean of the normalised rows is
+// taken first and the affine part applied once.  Each thread owns 8 columns per
+// step (one 16-byte load per row).  RAW = true writes plain span sums of the raw
+// rows instead (the bit-exact index check).
+// =====================================================================
+template <bool RAW>
+__global__ void __launch_bounds__(256) span_pool_kernel(SpanPoolArgs a) {
+    const int kind = a.item_kind[blockIdx.x];
+    const int idx = a.item_index[blockIdx.x];
+    const int H = a.H;
+    const int n8 = H >> 3;
+    int b, s, e;
+    if (kind == 0) {
+        b = a.q_rec[idx]; s = a.q_span[2 * idx]; e = a.q_span[2 * idx + 1];
+    } else if (kind == 1) {
+        b = a.o_rec[idx]; s = a.o_span[2 * idx]; e = a.o_span[2 * idx + 1];
+    } else {
+        b = idx; s = a.lengths[b] - 1; e = s + 1;
+    }
+    const int64_t rec_base = int64_t(b) * a.Lpad;
+    const int stat_base = a.rec_row_off[b];
+    const float inv_n = 1.0f / float(e - s);
+    for (int c8 = threadIdx.x; c8 < n8; c8 += blockDim.x) {
+        float acc[8], lex[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { acc[k] = 0.f; lex[k] = 0.f; }
+        for (int t = s; t < e; ++t) {
+            uint4 w = __ldg(reinterpret_cast<const uint4*>(a.hidden + (rec_base + t) * a.row_stride) + c8);
+            float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                          bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+            if (RAW) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[k] += v[k];
+            } else {
+                const float m = a.mu[stat_base + t], rs = a.rstd[stat_base + t];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[k] += (v[k] - m) * rs;
+            }
+            if (kind == 1) {
+                const int id = a.token_ids[rec_base + t];
+                if (id >= 0 && id < a.vocab) {
+                    uint4 x = __ldg(reinterpret_cast<const uint4*>(a.lexical + int64_t(id) * H) + c8);
+                    lex[0] += bf16_lo(x.x); lex[1] += bf16_hi(x.x); lex[2] += bf16_lo(x.y); lex[3] += bf16_hi(x.y);
+                    lex[4] += bf16_lo(x.z); lex[5] += bf16_hi(x.z); lex[6] += bf16_lo(x.w); lex[7] += bf16_hi(x.w);
+                } else if (c8 == 0) {
+                    atomicOr(a.flags, kFlagBounds);
+                }
+            }
+        }
+        const int col = c8 * 8;
+        if (RAW) {
+            float* dst = kind == 0 ? a.q_sum + int64_t(idx) * H : (kind == 1 ? a.o_sum + int64_t(idx) * H : nullptr);
+            if (dst) {
+                reinterpret_cast<float4*>(dst + col)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                reinterpret_cast<float4*>(dst + col)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+            if (kind == 1) {
+                float* dx = a.x_sum + int64_t(idx) * H + col;
+                reinterpret_cast<float4*>(dx)[0] = make_float4(lex[0], lex[1], lex[2], lex[3]);
+                reinterpret_cast<float4*>(dx)[1] = make_float4(lex[4], lex[5], lex[6], lex[7]);
+            }
+            continue;
+        }
+        uint4 gw = __ldg(reinterpret_cast<const uint4*>(a.ln_w) + c8);
+        uint4 bw = __ldg(reinterpret_cast<const uint4*>(a.ln_b) + c8);
+        const float gam[8] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y),
+                              bf16_lo(gw.z), bf16_hi(gw.z), bf16_lo(gw.w), bf16_hi(gw.w)};
+        const float bet[8] = {bf16_lo(bw.x), bf16_hi(bw.x), bf16_lo(bw.y), bf16_hi(bw.y),
+                              bf16_lo(bw.z), bf16_hi(bw.z), bf16_lo(bw.w), bf16_hi(bw.w)};
+        float val[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) val[k] = acc[k] * inv_n * gam[k] + bet[k];
+        uint4 vb;
+        vb.x = pack_bf16(val[0], val[1]); vb.y = pack_bf16(val[2], val[3]);
+        vb.z = pack_bf16(val[4], val[5]); vb.w = pack_bf16(val[6], val[7]);
+        const float4 v0 = make_float4(val[0], val[1], val[2], val[3]);
+        const float4 v1 = make_float4(val[4], val[5], val[6], val[7]);
+        if (kind == 0) {
+            float* u = a.u32 + int64_t(idx) * H + col;
+            reinterpret_cast<float4*>(u)[0] = v0;
+            reinterpret_cast<float4*>(u)[1] = v1;
+            *reinterpret_cast<uint4*>(a.a_field + int64_t(idx) * a.ld_field + col) = vb;
+            for (int j = a.q_opt_off[idx]; j < a.q_opt_off[idx + 1]; ++j)
+                *reinterpret_cast<uint4*>(a.a_query + int64_t(j) * a.ld_query + 2 * H + col) = vb;
+        } else if (kind == 1) {
+            *reinterpret_cast<uint4*>(a.a_query + int64_t(idx) * a.ld_query + col) = vb;
+            if (a.dbg_c) {
+                reinterpret_cast<float4*>(a.dbg_c + int64_t(idx) * H + col)[0] = v0;
+                reinterpret_cast<float4*>(a.dbg_c + int64_t(idx) * H + col)[1] = v1;
+            }
+            float xv[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) xv[k] = lex[k] * inv_n;
+            float* x = a.x32 + int64_t(idx) * H + col;
+            reinterpret_cast<float4*>(x)[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+            reinterpret_cast<float4*>(x)[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+            uint4 xb;
+            xb.x = pack_bf16(xv[0], xv[1]); xb.y = pack_bf16(xv[2], xv[3]);
+            xb.z = pack_bf16(xv[4], xv[5]); xb.w = pack_bf16(xv[6], xv[7]);
+            *reinterpret_cast<uint4*>(a.a_query + int64_t(idx) * a.ld_query + H + col) = xb;
+        } else {
+            float* g = a.g32 + int64_t(idx) * H + col;
+            reinterpret_cast<float4*>(g)[0] = v0;
+            reinterpret_cast<float4*>(g)[1] = v1;
+            for (int q = a.rec_q_off[b]; q < a.rec_q_off[b + 1]; ++q)
+                *reinterpret_cast<uint4*>(a.a_field + int64_t(q) * a.ld_field + H + col) = vb;
+        }
+    }
+}
+
+// =====================================================================
+// LayerNorm of fp32 rows of width D (pre-LN of the routing / joint layers and the
+// final option / field norms).  One warp per row, two-pass statistics.
+// =====================================================================
+__global__ void __launch_bounds__(256) layer_norm_kernel(const float* __restrict__ x, int rows, int D,
+                                                        const uint16_t* __restrict__ w,
+                                                        const uint16_t* __restrict__ bias,
+                                                        uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= rows) return;
+    constexpr int kMax = 64;  // D <= 2048
+    float v[kMax];
+    const float* row = x + int64_t(r) * D;
+    const int n = D >> 5;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMax; ++i)
+        if (i < n) { v[i] = row[i * 32 + lane]; s += v[i]; }
+    const float m = warp_sum(s) / float(D);
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMax; ++i)
+        if (i < n) { const float d = v[i] - m; q += d * d; }
+    const float rs = rsqrtf(warp_sum(q) / float(D) + 1e-5f);
+#pragma unroll
+    for (int i = 0; i < kMax; ++i) {
+        if (i < n) {
+            const int c = i * 32 + lane;
+            const float y = (v[i] - m) * rs * bf16_to_float(w[c]) + bf16_to_float(bias[c]);
+            if (out_bf16) out_bf16[int64_t(r) * D + c] = float_to_bf16(y);
+            if (out_f32) out_f32[int64_t(r) * D + c] = y;
+        }
+    }
+}
+
+// =====================================================================
+// Routing cross-attention, split over the memory length ("clef-4bit JointSchemaHead
+// walkthrough" section 3 step 2: every option queries the whole memory).
+// One CTA per (record chunk of kAttnChunk keys, head).  8 warps take 16 option
+// queries each (128 per pass; more passes for larger records).  K/V tiles of 64
+// keys stream through a double-buffered, XOR-swizzled shared-memory ring with
+// cp.async; QK^T and PV run on mma.sync bf16 tensor cores with an online softmax
+// (exp2 domain).  Keys at or past the chunk end are zero-filled and masked.
+// Each (option, head, chunk) leaves (max, sum, unnormalised accumulator).
+// =====================================================================
+namespace {
+constexpr int kKT = 64;  // keys per tile
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a [rows][64 bf16] tile
+    return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+}  // namespace
+
+__global__ void __launch_bounds__(256) route_attn_partial_kernel(RouteAttnArgs a) {
+    __shared__ __align__(128) uint8_t sQ[128 * 128];
+    __shared__ __align__(128) uint8_t sK[2][kKT * 128];
+    __shared__ __align__(128) uint8_t sV[2][kKT * 128];
+
+    const int cx = blockIdx.x, h = blockIdx.y;
+    const int b = a.chunk_rec[cx], kc = a.chunk_idx[cx];
+    const int L = a.lengths[b];
+    const int t0 = kc * kAttnChunk;
+    const int t1 = min(t0 + kAttnChunk, L);
+    const int n_tiles = (t1 - t0 + kKT - 1) / kKT;
+    const int o_base = a.rec_o_off[b];
+    const int O_b = a.rec_o_off[b + 1] - o_base;
+    const int64_t kv_row0 = a.rec_row_off[b];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const float sl2 = a.scale_log2;
+    const int64_t part_base = a.rec_part_off[b] + (int64_t(kc) * a.heads + h) * O_b;
+
+    auto load_kv = [&](int tile, int buf) {
+        // 64 rows x 8 chunks for K and for V: 1024 16-byte copies, 4 per thread
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int id = threadIdx.x + i * 256;
+            const int which = id >> 9;  // 0 = K, 1 = V
+            const int row = (id >> 3) & 63, ch = id & 7;
+            const int t = t0 + tile * kKT + row;
+            const bool valid = t < t1;
+            const uint16_t* src = a.kv + (kv_row0 + (valid ? t : t0)) * a.ldkv + (which ? a.v_col : a.k_col) +
+                                  h * 64 + ch * 8;
+            uint8_t* dst = (which ? sV[buf] : sK[buf]) + swz(row, ch);
+            cp_async16(dst, src, valid);
+        }
+    };
+
+    for (int qp = 0; qp * 128 < O_b; ++qp) {
+        // Q tile: 128 rows x 8 chunks
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int id = threadIdx.x + i * 256;
+            const int row = id >> 3, ch = id & 7;
+            const int o = qp * 128 + row;
+            const bool valid = o < O_b;
+            const uint16_t* src = a.q + int64_t(o_base + (valid ? o : 0)) * a.ldq + h * 64 + ch * 8;
+            cp_async16(sQ + swz(row, ch), src, valid);
+        }
+        load_kv(0, 0);
+        cp_async_commit();
+
+        const int wrow0 = warp * 16;
+        const bool active = qp * 128 + wrow0 < O_b;
+        uint32_t qa[4][4];
+        float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+        float acc[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+        for (int kt = 0; kt < n_tiles; ++kt) {
+            if (kt + 1 < n_tiles) load_kv(kt + 1, (kt + 1) & 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+            __syncthreads();
+            if (kt == 0 && active) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const int row = wrow0 + (lane & 15);
+                    const int ch = ks * 2 + (lane >> 4);
+                    ldmatrix_x4(qa[ks], smem_u32(sQ) + swz(row, ch));
+                }
+            }
+            if (active) {
+                const uint8_t* kb = sK[kt & 1];
+                const uint8_t* vb = sV[kt & 1];
+                float s[8][4];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                    for (int jp = 0; jp < 4; ++jp) {  // pairs of 8-key n-tiles
+                        uint32_t kr[4];
+                        const int key = jp * 16 + (lane & 7) + ((lane >> 4) << 3);
+                        const int ch = ks * 2 + ((lane >> 3) & 1);
+                        ldmatrix_x4(kr, smem_u32(kb) + swz(key, ch));
+                        mma_bf16_16816(s[2 * jp], qa[ks], kr[0], kr[1]);
+                        mma_bf16_16816(s[2 * jp + 1], qa[ks], kr[2], kr[3]);
+                    }
+                }
+                // scale, mask, online softmax
+                const int kbase = t0 + kt * kKT;
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int key = kbase + j * 8 + tq * 2 + (c & 1);
+                        const float v = key < t1 ? s[j][c] * sl2 : -INFINITY;
+                        s[j][c] = v;
+                        mx[c >> 1] = fmaxf(mx[c >> 1], v);
+                    }
+                }
+                float corr[2], ps[2] = {0.f, 0.f};
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                    const float mn = fmaxf(m_r[r], mx[r]);
+                    corr[r] = exp2f(m_r[r] - mn);
+                    m_r[r] = mn;
+                }
+                uint32_t pa[4][4];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float p0 = exp2f(s[j][0] - m_r[0]), p1 = exp2f(s[j][1] - m_r[0]);
+                    const float p2 = exp2f(s[j][2] - m_r[1]), p3 = exp2f(s[j][3] - m_r[1]);
+                    ps[0] += p0 + p1;
+                    ps[1] += p2 + p3;
+                    pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
+                    pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) l_r[r] = l_r[r] * corr[r] + ps[r];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc[j][0] *= corr[0]; acc[j][1] *= corr[0];
+                    acc[j][2] *= corr[1]; acc[j][3] *= corr[1];
+                }
+                // P (16 x 64 keys) * V (64 keys x 64 dims)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    // A fragment order: (row g, keys lo), (row g+8, keys lo), (row g, keys hi), (row g+8, keys hi)
+                    uint32_t af[4] = {pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3]};
+#pragma unroll
+                    for (int dp = 0; dp < 4; ++dp) {  // pairs of 8-dim n-tiles
+                        uint32_t vr[4];
+                        const int key = ks * 16 + (lane & 15);
+                        const int ch = dp * 2 + (lane >> 4);
+                        ldmatrix_x4_trans(vr, smem_u32(vb) + swz(key, ch));
+                        mma_bf16_16816(acc[2 * dp], af, vr[0], vr[1]);
+                        mma_bf16_16816(acc[2 * dp + 1], af, vr[2], vr[3]);
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        // per-row totals across the quad, then write the partials
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
+            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
+        }
+        if (active) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int o = qp * 128 + wrow0 + g + r * 8;
+                if (o < O_b) {
+                    const int64_t pi = part_base + o;
+                    if (tq == 0) {
+                        a.pm[pi] = m_r[r];
+                        a.pl[pi] = l_r[r];
+                    }
+                    float* dst = a.pacc + pi * 64;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float2*>(dst + j * 8 + tq * 2) = make_float2(acc[j][2 * r], acc[j][2 * r + 1]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Merge of the split-L partials of one (option, head): one warp, 2 dims per lane.
+__global__ void __launch_bounds__(256) route_attn_merge_kernel(RouteAttnArgs a, int O) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + warp;
+    if (item >= O * a.heads) return;
+    const int o = item / a.heads, h = item % a.heads;
+    const int b = a.o_rec[o];
+    const int o_base = a.rec_o_off[b];
+    const int O_b = a.rec_o_off[b + 1] - o_base;
+    const int nch = (a.lengths[b] + kAttnChunk - 1) / kAttnChunk;
+    float M = -INFINITY;
+    for (int k = 0; k < nch; ++k)
+        M = fmaxf(M, a.pm[a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base)]);
+    float Ls = 0.f, x0 = 0.f, x1 = 0.f;
+    for (int k = 0; k < nch; ++k) {
+        const int64_t pi = a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base);
+        const float w = exp2f(a.pm[pi] - M);
+        Ls += a.pl[pi] * w;
+        const float2 v = *reinterpret_cast<const float2*>(a.pacc + pi * 64 + lane * 2);
+        x0 += v.x * w;
+        x1 += v.y * w;
+    }
+    const float inv = 1.0f / Ls;
+    *reinterpret_cast<uint32_t*>(a.out + int64_t(o) * a.ldo + h * 64 + lane * 2) = pack_bf16(x0 * inv, x1 * inv);
+}
+
+// =====================================================================
+// Field aggregation, summary part ("clef-4bit JointSchemaHead walkthrough" section 3
+// step 3, option-weighted summary): alpha = softmax_j(w_a . o_hat_j + b_a) over
+// the question's options; summary = sum_j alpha_j o_hat_j, written as bf16 into
+// the field projection's input row.  One CTA per question.
+// =====================================================================
+__global__ void __launch_bounds__(256) field_pool_kernel(const float* __restrict__ o_hat, int D,
+                                                        const int32_t* __restrict__ q_opt_off,
+                                                        const uint16_t* __restrict__ w_a, const uint16_t* __restrict__ b_a,
+                                                        uint16_t* __restrict__ out, int64_t ldo, int col_off) {
+    __shared__ float sc[256];
+    const int q = blockIdx.x;
+    const int j0 = q_opt_off[q], n = q_opt_off[q + 1] - j0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < n; j += 8) {
+        const float* row = o_hat + int64_t(j0 + j) * D;
+        float s = 0.f;
+        for (int c = lane; c < D; c += 32) s += row[c] * bf16_to_float(w_a[c]);
+        s = warp_sum(s);
+        if (lane == 0) sc[j] = s + bf16_to_float(b_a[0]);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float m = -INFINITY;
+        for (int j = lane; j < n; j += 32) m = fmaxf(m, sc[j]);
+        m = warp_max(m);
+        float z = 0.f;
+        for (int j = lane; j < n; j += 32) z += expf(sc[j] - m);
+        z = warp_sum(z);
+        __syncwarp();
+        for (int j = lane; j < n; j += 32) sc[j] = expf(sc[j] - m) / z;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float s = 0.f;
+        for (int j = 0; j < n; ++j) s += sc[j] * o_hat[int64_t(j0 + j) * D + c];
+        out[int64_t(q) * ldo + col_off + c] = float_to_bf16(s);
+    }
+}
+
+// =====================================================================
+// Self-attention among one record's fields (joint layers, "clef-4bit JointSchemaHead
+// walkthrough" section 3 step 3: fields are mutually visible).  One CTA per
+// (record, head); fp32 scores and softmax; at most kMaxFields fields per record.
+// qkv is bf16 [Q][3D] (q | k | v), out bf16 [Q][D].
+// =====================================================================
+__global__ void __launch_bounds__(128) field_attn_kernel(const uint16_t* __restrict__ qkv, int D,
+                                                        const int32_t* __restrict__ rec_q_off, float scale,
+                                                        uint16_t* __restrict__ out) {
+    __shared__ float sq[kMaxFields][65], sk[kMaxFields][65], sv[kMaxFields][65];
+    __shared__ float sp[kMaxFields][kMaxFields + 1];
+    const int b = blockIdx.x, h = blockIdx.y;
+    const int q0 = rec_q_off[b], n = rec_q_off[b + 1] - q0;
+    for (int i = threadIdx.x; i < n * 64; i += blockDim.x) {
+        const int r = i >> 6, c = i & 63;
+        const uint16_t* row = qkv + int64_t(q0 + r) * 3 * D + h * 64 + c;
+        sq[r][c] = bf16_to_float(row[0]);
+        sk[r][c] = bf16_to_float(row[D]);
+        sv[r][c] = bf16_to_float(row[2 * D]);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n * n; i += blockDim.x) {
+        const int r = i / n, c = i % n;
+        float s = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < 64; ++d) s += sq[r][d] * sk[c][d];
+        sp[r][c] = s * scale;
+    }
+    __syncthreads();
+    if (threadIdx.x < n) {
+        const int r = threadIdx.x;
+        float m = -INFINITY;
+        for (int c = 0; c < n; ++c) m = fmaxf(m, sp[r][c]);
+        float z = 0.f;
+        for (int c = 0; c < n; ++c) { const float e = expf(sp[r][c] - m); sp[r][c] = e; z += e; }
+        const float inv = 1.f / z;
+        for (int c = 0; c < n; ++c) sp[r][c] *= inv;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n * 64; i += blockDim.x) {
+        const int r = i >> 6, d = i & 63;
+        float s = 0.f;
+        for (int c = 0; c < n; ++c) s += sp[r][c] * sv[c][d];
+        out[int64_t(q0 + r) * D + h * 64 + d] = float_to_bf16(s);
+    }
+}
+
+// =====================================================================
+// Scorer MLP input ("clef-4bit JointSchemaHead walkthrough" section 3 step 4):
+// z_j = [f_hat_q, o_hat_j, f_hat_q * o_hat_j, |f_hat_q - o_hat_j|], bf16 [O][4D].
+// =====================================================================
+__global__ void __launch_bounds__(256) build_z_kernel(const float* __restrict__ f_hat, const float* __restrict__ o_hat,
+                                                     const int32_t* __restrict__ o_q, int O, int D,
+                                                     uint16_t* __restrict__ z) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= int64_t(O) * D) return;
+    const int j = int(i / D), c = int(i % D);
+    const float f = f_hat[int64_t(o_q[j]) * D + c], o = o_hat[i];
+    uint16_t* row = z + int64_t(j) * 4 * D;
+    row[c] = float_to_bf16(f);
+    row[D + c] = float_to_bf16(o);
+    row[2 * D + c] = float_to_bf16(f * o);
+    row[3 * D + c] = float_to_bf16(fabsf(f - o));
+}
+
+// =====================================================================
+// Scoring and per-question softmax, one CTA per question
+// ("clef-4bit JointSchemaHead walkthrough" section 3 step 4;
+// "clef-flash-CoreAI metadata.json" decision.softmax and decision.response):
+//   logit_j = cos(x_j, u_q + g_b) + sigmoid(gate) * (joint_scale * cos(f_hat_q, o_hat_j) + mlp_j)
+//   mlp_j   = w2 . hidden_j + b2  (hidden_j = GELU(W1 z_j + b1) from the GEMM)
+//   p = softmax over the question's options; answers by question type.
+// =====================================================================
+__global__ void __launch_bounds__(256) score_softmax_kernel(ScoreArgs a) {
+    __shared__ float s_logit[256];
+    __shared__ float s_red[8];
+    __shared__ float s_anchor_norm;
+    const int q = blockIdx.x;
+    const int b = a.q_rec[q];
+    const int j0 = a.q_opt_off[q], n = a.q_opt_off[q + 1] - j0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, D = a.D;
+    const float* u = a.u32 + int64_t(q) * H;
+    const float* g = a.g32 + int64_t(b) * H;
+    // |u_q + g_b|
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) { const float v = u[c] + g[c]; ss += v * v; }
+    ss = warp_sum(ss);
+    if (lane == 0) s_red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += s_red[w];
+        s_anchor_norm = fmaxf(sqrtf(t), 1e-8f);
+    }
+    __syncthreads();
+    const float gate = 1.0f / (1.0f + expf(-bf16_to_float(a.gate[0])));
+    const float jscale = bf16_to_float(a.joint_scale[0]);
+    const float* f = a.f_hat + int64_t(q) * D;
+    for (int jj = warp; jj < n; jj += 8) {
+        const int j = j0 + jj;
+        const float* x = a.x32 + int64_t(j) * H;
+        float xa = 0.f, xx = 0.f;
+        for (int c = lane; c < H; c += 32) { const float xv = x[c]; xa += xv * (u[c] + g[c]); xx += xv * xv; }
+        const float* o = a.o_hat + int64_t(j) * D;
+        const uint16_t* hm = a.mlp_hidden + int64_t(j) * D;
+        float fo = 0.f, ff = 0.f, oo = 0.f, mm = 0.f;
+        for (int c = lane; c < D; c += 32) {
+            const float fv = f[c], ov = o[c];
+            fo += fv * ov; ff += fv * fv; oo += ov * ov;
+            mm += bf16_to_float(hm[c]) * bf16_to_float(a.w2[c]);
+        }
+        xa = warp_sum(xa); xx = warp_sum(xx); fo = warp_sum(fo); ff = warp_sum(ff); oo = warp_sum(oo); mm = warp_sum(mm);
+        if (lane == 0) {
+            const float prior = xa / (fmaxf(sqrtf(xx), 1e-8f) * s_anchor_norm);
+            const float joint = fo / (fmaxf(sqrtf(ff), 1e-8f) * fmaxf(sqrtf(oo), 1e-8f));
+            const float mlp = mm + bf16_to_float(a.b2[0]);
+            s_logit[jj] = prior + gate * (jscale * joint + mlp);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float m = -INFINITY;
+        for (int j = lane; j < n; j += 32) m = fmaxf(m, s_logit[j]);
+        m = warp_max(m);
+        float z = 0.f;
+        for (int j = lane; j < n; j += 32) z += expf(s_logit[j] - m);
+        z = warp_sum(z);
+        float ev = 0.f;
+        for (int j = lane; j < n; j += 32) {
+            const float p = expf(s_logit[j] - m) / z;
+            a.logits[j0 + j] = s_logit[j];
+            a.probs[j0 + j] = p;
+            ev += float(j) * p;
+        }
+        ev = warp_sum(ev);
+        if (lane == 0) {
+            // first maximum in option order (ties -> lowest index)
+            int k = 0;
+            for (int j = 1; j < n; ++j)
+                if (s_logit[j] > s_logit[k]) k = j;
+            const float pk = expf(s_logit[k] - m) / z;
+            const int t = a.q_type[q];
+            a.q_argmax[q] = k;
+            a.q_conf[q] = pk;
+            a.q_value[q] = t == 0 ? expf(s_logit[0] - m) / z : (t == 1 ? pk : ev);
+        }
+    }
+}
+
+// =====================================================================
+// Weight preparation.
+// Memory K/V projections with the memory LayerNorm folded in: for weight row n,
+//   W'[n][k] = bf16(W[n][k] * gamma[k]),  c[n] = sum_k W'[n][k],
+//   b'[n] = sum_k beta[k] * W[n][k] + bias[n]
+// so that W LN(h) + bias = rstd * (W' h - mu c) + b'.
+// =====================================================================
+__global__ void __launch_bounds__(256) fold_kv_kernel(FoldArgs a) {
+    __shared__ float red[2][8];
+    const int n = blockIdx.x;
+    const int mat = n / a.D, r = n % a.D;
+    const uint16_t* W = a.w[mat] + int64_t(r) * a.H;
+    uint16_t* Wp = a.out_w + int64_t(n) * a.H;
+    float cs = 0.f, bs = 0.f;
+    for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
+        const float w = bf16_to_float(W[k]);
+        const uint16_t wp = float_to_bf16(w * bf16_to_float(a.gamma[k]));
+        Wp[k] = wp;
+        cs += bf16_to_float(wp);
+        bs += w * bf16_to_float(a.beta[k]);
+    }
+    cs = warp_sum(cs);
+    bs = warp_sum(bs);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) { red[0][warp] = cs; red[1][warp] = bs; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float c = 0.f, bb = 0.f;
+        for (int w = 0; w < 8; ++w) { c += red[0][w]; bb += red[1][w]; }
+        a.out_c[n] = c;
+        a.out_b[n] = bb + bf16_to_float(a.bias[mat][r]);
+    }
+}
+
+// dst[r][col_off + c] = src[r][c] for a [rows][cols] bf16 block (16-byte units).
+__global__ void __launch_bounds__(256) copy_cols_kernel(uint16_t* __restrict__ dst, int64_t ld_dst, int col_off,
+                                                       const uint16_t* __restrict__ src, int64_t ld_src, int rows,
+                                                       int cols) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int c8 = cols >> 3;
+    if (i >= int64_t(rows) * c8) return;
+    const int r = int(i / c8), c = int(i % c8) * 8;
+    *reinterpret_cast<uint4*>(dst + int64_t(r) * ld_dst + col_off + c) =
+        *reinterpret_cast<const uint4*>(src + int64_t(r) * ld_src + c);
+}
+
+// ----------------------------------------------------------------- launchers
+
+cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpad, int H, const int32_t* tile_rec,
+                             const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,
+                             cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    row_stats_kernel<<<(R + 7) / 8, 256, 0, s>>>(hidden, row_stride, Lpad, H, tile_rec, rec_row_off, lengths, R, mu,
+                                                 rstd);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s) {
+    if (n_items <= 0) return cudaSuccess;
+    if (raw) span_pool_kernel<true><<<n_items, 256, 0, s>>>(a);
+    else span_pool_kernel<false><<<n_items, 256, 0, s>>>(a);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
+                              uint16_t* out_bf16, float* out_f32, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    layer_norm_kernel<<<(rows + 7) / 8, 256, 0, s>>>(x, rows, D, w, b, out_bf16, out_f32);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, cudaStream_t s) {
+    if (n_chunks <= 0) return cudaSuccess;
+    route_attn_partial_kernel<<<dim3(n_chunks, a.heads), 256, 0, s>>>(a);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s) {
+    if (O <= 0) return cudaSuccess;
+    route_attn_merge_kernel<<<(O * a.heads + 7) / 8, 256, 0, s>>>(a, O);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,
+                              const uint16_t* b_a, uint16_t* out, int64_t ldo, int col_off, cudaStream_t s) {
+    if (Q <= 0) return cudaSuccess;
+    field_pool_kernel<<<Q, 256, 0, s>>>(o_hat, D, q_opt_off, w_a, b_a, out, ldo, col_off);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_field_attn(const uint16_t* qkv, int D, int heads, const int32_t* rec_q_off, int B, float scale,
+                              uint16_t* out, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    field_attn_kernel<<<dim3(B, heads), 128, 0, s>>>(qkv, D, rec_q_off, scale, out);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_build_z(const float* f_hat, const float* o_hat, const int32_t* o_q, int O, int D, uint16_t* z,
+                           cudaStream_t s) {
+    const int64_t n = int64_t(O) * D;
+    if (n <= 0) return cudaSuccess;
+    build_z_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(f_hat, o_hat, o_q, O, D, z);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s) {
+    if (Q <= 0) return cudaSuccess;
+    score_softmax_kernel<<<Q, 256, 0, s>>>(a);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_fold_kv(const FoldArgs& a, int rows, cudaStream_t s) {
+    fold_kv_kernel<<<rows, 256, 0, s>>>(a);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_copy_cols(uint16_t* dst, int64_t ld_dst, int col_off, const uint16_t* src, int64_t ld_src,
+                             int rows, int cols, cudaStream_t s) {
+    const int64_t n = int64_t(rows) * (cols / 8);
+    if (n <= 0) return cudaSuccess;
+    copy_cols_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(dst, ld_dst, col_off, src, ld_src, rows, cols);
+    return counted(cudaGetLastError());
+}
+
+}  // namespace clef

@@ -1,0 +1,83 @@
+// Argument blocks and launchers of the head's non-GEMM kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace clef {
+
+constexpr int kAttnChunk = 1024;  // memory rows per split-L routing-attention work item
+constexpr int kMaxFields = 48;    // questions per record handled by the field self-attention kernel
+constexpr int kMaxOptions = 256;  // options per question
+
+struct SpanPoolArgs {
+    const uint16_t* hidden; int64_t row_stride; int Lpad; int H; int vocab;
+    const int32_t* token_ids; const uint16_t* lexical;
+    const float* mu; const float* rstd;          // compact-row statistics
+    const uint16_t* ln_w; const uint16_t* ln_b;  // memory LayerNorm affine
+    const int32_t* item_kind; const int32_t* item_index;
+    const int32_t* lengths; const int32_t* rec_row_off; const int32_t* rec_q_off;
+    const int32_t* q_rec; const int32_t* q_span; const int32_t* q_opt_off;
+    const int32_t* o_rec; const int32_t* o_span;
+    // pooled outputs
+    uint16_t* a_query; int64_t ld_query;  // [O][3H]: c | x | u_q(j)
+    uint16_t* a_field; int64_t ld_field;  // [Q][2H + D]: u | g | summary
+    float* u32; float* x32; float* g32;   // fp32 copies for the scorer
+    float* dbg_c;                         // optional [O][H]
+    // raw-sum mode
+    float* q_sum; float* o_sum; float* x_sum;
+    int* flags;
+};
+
+struct RouteAttnArgs {
+    const uint16_t* q; int64_t ldq;       // [O][D] bf16 queries
+    const uint16_t* kv; int64_t ldkv;     // [R][ldkv] bf16 memory keys / values
+    int k_col, v_col;                     // column of this layer's K and V blocks
+    int heads;
+    float scale_log2;                     // log2(e) / sqrt(head dim)
+    const int32_t* chunk_rec; const int32_t* chunk_idx;
+    const int32_t* lengths; const int32_t* rec_row_off; const int32_t* rec_o_off;
+    const int64_t* rec_part_off;
+    const int32_t* o_rec;
+    float* pm; float* pl; float* pacc;    // partials
+    uint16_t* out; int64_t ldo;           // [O][D] bf16 merged output
+};
+
+struct ScoreArgs {
+    int H, D;
+    const int32_t* q_rec; const int32_t* q_type; const int32_t* q_opt_off;
+    const float* u32; const float* g32; const float* x32;
+    const float* f_hat; const float* o_hat;
+    const uint16_t* mlp_hidden;           // [O][D] bf16, GELU(W1 z + b1)
+    const uint16_t* w2; const uint16_t* b2; const uint16_t* gate; const uint16_t* joint_scale;
+    float* logits; float* probs; float* q_value; float* q_conf; int32_t* q_argmax;
+};
+
+struct FoldArgs {
+    int H, D;
+    const uint16_t* w[8];                 // K / V weights of every routing layer, [D][H]
+    const uint16_t* bias[8];
+    const uint16_t* gamma; const uint16_t* beta;
+    uint16_t* out_w; float* out_c; float* out_b;
+};
+
+cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpad, int H, const int32_t* tile_rec,
+                             const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,
+                             cudaStream_t s);
+cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s);
+cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
+                              uint16_t* out_bf16, float* out_f32, cudaStream_t s);
+cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, cudaStream_t s);
+cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s);
+cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,
+                              const uint16_t* b_a, uint16_t* out, int64_t ldo, int col_off, cudaStream_t s);
+cudaError_t launch_field_attn(const uint16_t* qkv, int D, int heads, const int32_t* rec_q_off, int B, float scale,
+                              uint16_t* out, cudaStream_t s);
+cudaError_t launch_build_z(const float* f_hat, const float* o_hat, const int32_t* o_q, int O, int D, uint16_t* z,
+                           cudaStream_t s);
+cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s);
+cudaError_t launch_fold_kv(const FoldArgs& a, int rows, cudaStream_t s);
+cudaError_t launch_copy_cols(uint16_t* dst, int64_t ld_dst, int col_off, const uint16_t* src, int64_t ld_src,
+                             int rows, int cols, cudaStream_t s);
+
+}  // namespace clef

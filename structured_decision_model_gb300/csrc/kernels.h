@@ -1,0 +1,60 @@
+// Host-side launchers of the head's kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace clef {
+
+// Kernels launched by the library since it was loaded.
+extern std::atomic<uint64_t> g_kernel_launches;
+
+// Counts a launch that the runtime accepted and passes the launch status on.
+inline cudaError_t counted(cudaError_t e) {
+    if (e == cudaSuccess) g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+    return e;
+}
+
+// ------------------------------------------------------------------ the GEMM
+
+enum EpiKind : int {
+    EPI_F32 = 0,        // out_f32 = acc + bias (+ table[row_idx[m]])
+    EPI_F32_RESID = 1,  // out_f32 += acc + bias  (residual stream update)
+    EPI_BF16 = 2,       // out_bf16 = act(acc + bias)
+    EPI_KV_LNFOLD = 3,  // out_bf16 = rstd[m] * (acc - mu[m] * col_c[n]) + bias_f32[n]
+};
+
+struct GemmEpilogue {
+    int kind = EPI_F32;
+    int gelu = 0;
+    const uint16_t* bias_bf16 = nullptr;  // [N]
+    const float* bias_f32 = nullptr;      // [N]
+    const float* row_mu = nullptr;        // [rows] (LN fold)
+    const float* row_rstd = nullptr;      // [rows] (LN fold)
+    const float* col_c = nullptr;         // [N]    (LN fold)
+    const uint16_t* row_table = nullptr;  // [*, N] bf16 rows added by index (type embedding)
+    const int32_t* row_idx = nullptr;     // [rows]
+    int64_t ld_table = 0;
+    void* out = nullptr;
+    int64_t ldo = 0;
+    int M = 0;  // rows that are stored (m < M)
+};
+
+struct GemmProblem {
+    const uint16_t* A = nullptr;  // bf16 [a_rows, K], row stride lda
+    int64_t lda = 0;
+    int64_t a_rows = 0;           // rows addressable through A's tensor map
+    const uint16_t* B = nullptr;  // bf16 [N, K], row stride ldb
+    int64_t ldb = 0;
+    int N = 0, K = 0;
+    int n_mtiles = 0;                        // 128-row output tiles
+    const int32_t* a_row_of_mtile = nullptr; // device [n_mtiles]: first A row of each tile (null: 128 * tile)
+};
+
+int num_sms();
+cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_flags, cudaStream_t s,
+                        int force_bn = 0);
+
+}  // namespace clef

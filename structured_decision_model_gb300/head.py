@@ -1,0 +1,98 @@
+"""PyTorch-side helper around the C ABI: device buffers and streams only.
+
+``ClefHead`` uploads a weight set, runs ``clef_prepare_weights`` once, and calls
+``clef_head_forward`` with torch-allocated device buffers on torch's current
+stream.  All arithmetic of the head happens in libclef_head.so.
+"""
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def weight_order(H, D, heads, F, n_route, n_joint):
+    """Names of the weight pointer table, in the order the C header documents."""
+    names = ["mem_ln.weight", "mem_ln.bias", "query.ctx.weight", "query.lex.weight",
+             "query.question.weight", "query.bias"]
+    for l in range(n_route):
+        names += [f"route.{l}.{k}" for k in (
+            "attn_ln.weight", "attn_ln.bias", "q.weight", "q.bias", "k.weight", "k.bias", "v.weight", "v.bias",
+            "o.weight", "o.bias", "ffn_ln.weight", "ffn_ln.bias", "ffn1.weight", "ffn1.bias", "ffn2.weight",
+            "ffn2.bias")]
+    names += ["option_ln.weight", "option_ln.bias", "field.pool.weight", "field.pool.bias",
+              "field.question.weight", "field.summary.weight", "field.global.weight", "field.bias",
+              "field.type_embedding"]
+    for i in range(n_joint):
+        names += [f"joint.{i}.{k}" for k in (
+            "attn_ln.weight", "attn_ln.bias", "qkv.weight", "qkv.bias", "o.weight", "o.bias", "ffn_ln.weight",
+            "ffn_ln.bias", "ffn1.weight", "ffn1.bias", "ffn2.weight", "ffn2.bias")]
+    names += ["field_ln.weight", "field_ln.bias", "scorer.gate", "scorer.joint_scale", "scorer.mlp1.weight",
+              "scorer.mlp1.bias", "scorer.mlp2.weight", "scorer.mlp2.bias"]
+    return names
+
+
+def to_device_bf16(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """uint16 bf16 bit patterns -> a torch bfloat16 tensor on ``device``."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def stream_handle(stream: Optional[torch.cuda.Stream] = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+@dataclass
+class Outputs:
+    logits: torch.Tensor
+    probs: torch.Tensor
+    q_value: torch.Tensor
+    q_conf: torch.Tensor
+    q_argmax: torch.Tensor
+
+
+class ClefHead:
+    def __init__(self, weights: dict, H=4096, D=1024, heads=16, F=4096, n_route=2, n_joint=4, vocab=248320,
+                 device="cuda"):
+        self.cfg = B.make_config(H, D, heads, F, n_route, n_joint, vocab)
+        self.H, self.D, self.heads, self.F, self.vocab = H, D, heads, F, vocab
+        self.device = device
+        names = weight_order(H, D, heads, F, n_route, n_joint)
+        if B.clef_weight_count(self.cfg) != len(names):
+            raise RuntimeError("weight table size mismatch with the C library")
+        self.weights = [to_device_bf16(weights[n], device) for n in names]
+        self.weight_ptrs = [w.data_ptr() for w in self.weights]
+        nbytes = B.clef_prepared_size(self.cfg)
+        self.prepared = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        B.clef_prepare_weights(self.cfg, self.weight_ptrs, self.prepared.data_ptr(), nbytes, stream_handle())
+        self._ws = None
+
+    def workspace(self, schema: B.Schema) -> torch.Tensor:
+        n = B.clef_workspace_size(self.cfg, schema)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def alloc_outputs(self, schema: B.Schema) -> Outputs:
+        dev = self.device
+        return Outputs(torch.empty(schema.O, dtype=torch.float32, device=dev),
+                       torch.empty(schema.O, dtype=torch.float32, device=dev),
+                       torch.empty(schema.Q, dtype=torch.float32, device=dev),
+                       torch.empty(schema.Q, dtype=torch.float32, device=dev),
+                       torch.empty(schema.Q, dtype=torch.int32, device=dev))
+
+    def forward(self, schema: B.Schema, hidden: torch.Tensor, token_ids: torch.Tensor, lexical: torch.Tensor,
+                out: Optional[Outputs] = None, debug=None, stream=None, check=True) -> Outputs:
+        ws = self.workspace(schema)
+        out = out if out is not None else self.alloc_outputs(schema)
+        B.clef_head_forward(self.cfg, self.weight_ptrs, self.prepared.data_ptr(), schema, hidden.data_ptr(),
+                            token_ids.data_ptr(), lexical.data_ptr(), out.logits.data_ptr(), out.probs.data_ptr(),
+                            out.q_value.data_ptr(), out.q_conf.data_ptr(), out.q_argmax.data_ptr(), ws.data_ptr(),
+                            ws.numel(), debug=debug, stream=stream_handle(stream), check=check)
+        return out
+
+    def device_status(self, stream=None) -> int:
+        return B.clef_device_status(self._ws.data_ptr(), stream_handle(stream))

@@ -153,9 +153,17 @@ class Batch:
         return np.unique(np.concatenate(ids)) if ids else np.zeros(0, np.int32)
 
     def record_hidden(self, b: int) -> np.ndarray:
+        """Hidden rows [Lpad, H] of record b (drawn on demand when not held)."""
         if self.hidden is not None:
             return self.hidden[b]
         return draw_hidden_record(self.seed, b, self.Lpad, self.H, self.spec.row_scale)
+
+    def real_rows(self, b: int) -> np.ndarray:
+        """The real rows [L_b, H] of record b: the same values as the first L_b rows of
+        ``record_hidden(b)``, without drawing the padding."""
+        if self.hidden is not None:
+            return self.hidden[b, :self.lengths[b]]
+        return draw_hidden_record(self.seed, b, int(self.lengths[b]), self.H, self.spec.row_scale)
 
 
 def _draw_lengths(spec: BatchSpec, rng) -> np.ndarray:

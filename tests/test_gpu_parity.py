@@ -1,0 +1,224 @@
+"""GPU parity of the CUDA path against the fp64 oracle, through the C ABI.
+
+Small cases run the whole batch through the oracle; they span several GEMM tiles,
+several routing-attention chunks and ragged tails.  Index work (span / offset /
+gather) is checked bit for bit with small-integer inputs.
+"""
+import ctypes
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from structured_decision_model_gb300 import binding as B
+from structured_decision_model_gb300.build import build_library
+
+from gpu_support import compare, device_inputs, head_for, run_gpu, run_oracle, schema_of
+
+pytestmark = pytest.mark.gpu
+
+FULL = synth.HeadShape()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build_library()
+    B.load()
+    torch.cuda.init()
+
+
+# ------------------------------------------------------------------- GEMM
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (100, 1024, 1024), (129, 256, 512), (300, 4096, 1024),
+                                   (1000, 1024, 4096), (2048, 4096, 4096), (777, 3072, 1024), (64, 1024, 12288)])
+def test_gemm_matches_torch(M, N, K):
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N + K)
+    A = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=g).to(torch.bfloat16)
+    Bm = torch.randn((N, K), dtype=torch.float32, device="cuda", generator=g).to(torch.bfloat16)
+    bias = torch.randn(N, dtype=torch.float32, device="cuda", generator=g)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.clef_gemm_bf16(A.data_ptr(), K, Bm.data_ptr(), K, bias.data_ptr(), C.data_ptr(), N, M, N, K,
+                     flags.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    ref = A.float() @ Bm.float().T + bias
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    err = (C - ref).abs().max().item()
+    scale = ref.abs().max().item()
+    assert err <= 1e-3 * scale + 1e-3, (err, scale)
+
+
+def test_gemm_strided_operands():
+    M, N, K, lda, ldb = 250, 512, 320, 328, 400
+    g = torch.Generator(device="cuda").manual_seed(5)
+    A = torch.randn((M, lda), dtype=torch.float32, device="cuda", generator=g).to(torch.bfloat16)
+    Bm = torch.randn((N, ldb), dtype=torch.float32, device="cuda", generator=g).to(torch.bfloat16)
+    C = torch.full((M, N + 64), 7.0, dtype=torch.float32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.clef_gemm_bf16(A.data_ptr(), lda, Bm.data_ptr(), ldb, None, C.data_ptr(), N + 64, M, N, K,
+                     flags.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    ref = A[:, :K].float() @ Bm[:, :K].float().T
+    torch.cuda.synchronize()
+    assert (C[:, :N] - ref).abs().max().item() <= 1e-3 * ref.abs().max().item()
+    assert bool((C[:, N:] == 7.0).all())  # nothing written past N
+
+
+# ------------------------------------------------------- index work, exact
+
+def test_span_sums_bit_exact_integer_inputs():
+    shape = synth.HeadShape(H=256, vocab=3000)
+    spec = synth.BatchSpec(name="int", B=4, H=256, vocab=3000, length_law="uniform", length_range=(200, 900),
+                           questions=(1, 6), options=(2, 7), instr_len=(1, 40), option_len=(1, 20))
+    bt = synth.make_batch(spec, seed=11, with_hidden=False)
+    rng = np.random.default_rng(3)
+    bt.hidden = synth.f32_to_bf16(rng.integers(-16, 17, size=(bt.B, bt.Lpad, bt.H)).astype(np.float32))
+    table = synth.f32_to_bf16(rng.integers(-8, 9, size=(shape.vocab, bt.H)).astype(np.float32))
+    hidden = torch.from_numpy(bt.hidden.view(np.int16)).cuda().view(torch.bfloat16)
+    lex = torch.from_numpy(table.view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.from_numpy(bt.token_ids).cuda()
+    cfg = B.make_config(H=256, vocab=3000)
+    sch = schema_of(bt)
+    nws = B.clef_workspace_size(cfg, sch)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    qs = torch.empty((bt.Q, bt.H), dtype=torch.float32, device="cuda")
+    os_ = torch.empty((bt.O, bt.H), dtype=torch.float32, device="cuda")
+    xs = torch.empty((bt.O, bt.H), dtype=torch.float32, device="cuda")
+    B.clef_span_sums(cfg, sch, hidden.data_ptr(), ids.data_ptr(), lex.data_ptr(), qs.data_ptr(), os_.data_ptr(),
+                     xs.data_ptr(), ws.data_ptr(), nws, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert B.clef_device_status(ws.data_ptr(), 0) == 0
+    q_all, o_all, x_all = [], [], []
+    for b in range(bt.B):
+        qsel = np.nonzero(bt.q_rec == b)[0]
+        lo, hi = bt.q_opt_off[qsel[0]], bt.q_opt_off[qsel[-1] + 1]
+        o_ids = [bt.token_ids[b][s:e] for (s, e) in bt.o_span[lo:hi]]
+        sq, so, sx = oracle.span_raw_sums(bt.hidden[b], bt.q_span[qsel], bt.o_span[lo:hi], o_ids, table)
+        q_all.append(sq); o_all.append(so); x_all.append(sx)
+    np.testing.assert_array_equal(qs.cpu().numpy(), np.concatenate(q_all).astype(np.float32))
+    np.testing.assert_array_equal(os_.cpu().numpy(), np.concatenate(o_all).astype(np.float32))
+    np.testing.assert_array_equal(xs.cpu().numpy(), np.concatenate(x_all).astype(np.float32))
+
+
+def test_out_of_range_token_id_is_reported():
+    shape = synth.HeadShape(H=256, vocab=3000)
+    spec = synth.BatchSpec(name="oob", B=2, H=256, vocab=3000, length_law="uniform", length_range=(300, 400),
+                           questions=(2, 3), options=(2, 4), instr_len=(3, 8), option_len=(2, 5))
+    bt = synth.make_batch(spec, seed=12)
+    head, w = head_for(shape)
+    bt.token_ids[bt.q_rec[0], bt.o_span[0, 0]] = shape.vocab + 5
+    hidden, ids, lex = device_inputs(bt, shape.vocab)
+    head.forward(schema_of(bt), hidden, ids, lex)
+    torch.cuda.synchronize()
+    assert head.device_status() == 5  # CLEF_ERR_DEVICE_BOUNDS
+    assert head.device_status() == 0  # reading clears it
+
+
+# ------------------------------------------------------- whole head, small
+
+def _debug_buffers(bt, shape):
+    z = lambda *s: torch.zeros(s, dtype=torch.float32, device="cuda")
+    bufs = dict(pooled_u=z(bt.Q, shape.H), pooled_c=z(bt.O, shape.H), pooled_x=z(bt.O, shape.H),
+                global_g=z(bt.B, shape.H), option_final=z(bt.O, shape.D), field_final=z(bt.Q, shape.D))
+    dbg = B.ClefDebugOutputs(*[bufs[k].data_ptr() for k in
+                               ("pooled_u", "pooled_c", "pooled_x", "global_g", "option_final", "field_final")])
+    return bufs, dbg
+
+
+def test_pr1_reference_record_full_head():
+    bt = synth.make_batch(synth.workload_spec("pr1_ref_b1_l512"), seed=1)
+    head, w = head_for(FULL)
+    bufs, dbg = _debug_buffers(bt, FULL)
+    gpu = run_gpu(head, bt, debug=dbg)
+    ref = run_oracle(w, FULL, bt, keep=True)
+    inter = ref["inter"][0]
+    np.testing.assert_allclose(bufs["pooled_u"].cpu().numpy(), inter["u"], atol=2e-4)
+    np.testing.assert_allclose(bufs["pooled_c"].cpu().numpy(), inter["c"], atol=2e-4)
+    np.testing.assert_allclose(bufs["pooled_x"].cpu().numpy(), inter["x"], atol=1e-6)
+    np.testing.assert_allclose(bufs["global_g"].cpu().numpy()[0], inter["g"], atol=2e-4)
+    np.testing.assert_allclose(bufs["option_final"].cpu().numpy(), inter["o_hat"], atol=5e-2)
+    np.testing.assert_allclose(bufs["field_final"].cpu().numpy(), inter["f_hat"], atol=5e-2)
+    compare(gpu, ref, bt)
+
+
+def ragged_spec(**kw):
+    d = dict(name="ragged", B=3, length_law="uniform", length_range=(700, 2600), questions=(3, 6),
+             options=(2, 7))
+    d.update(kw)
+    return synth.BatchSpec(**d)
+
+
+def test_ragged_batch_several_tiles_and_chunks():
+    bt = synth.make_batch(ragged_spec(), seed=5)
+    assert bt.lengths.max() > 1024 and (bt.lengths % 128 != 0).all()
+    head, w = head_for(FULL)
+    gpu = run_gpu(head, bt)
+    compare(gpu, run_oracle(w, FULL, bt), bt)
+
+
+def test_wide_backbone_small_batch():
+    shape = dataclasses.replace(FULL, H=5120)
+    bt = synth.make_batch(ragged_spec(H=5120, B=2, length_range=(600, 1500)), seed=6)
+    head, w = head_for(shape)
+    compare(run_gpu(head, bt), run_oracle(w, shape, bt), bt)
+
+
+def test_strided_hidden_rows():
+    bt = synth.make_batch(ragged_spec(B=2, length_range=(300, 900)), seed=7)
+    head, w = head_for(FULL)
+    compare(run_gpu(head, bt, row_stride=FULL.H + 64), run_oracle(w, FULL, bt), bt)
+
+
+def test_single_question_single_option_records():
+    spec = synth.BatchSpec(name="deg", B=3, lengths=[1, 2, 160], fixed_types=[(1, 1)], instr_len=(1, 1),
+                           option_len=(1, 1))
+    # a length-1 record cannot hold the synthetic layout: build the tables by hand
+    bt = synth.make_batch(dataclasses.replace(spec, lengths=[160, 160, 160]), seed=8)
+    bt = dataclasses.replace(bt, lengths=np.array([1, 2, 160], np.int32),
+                             q_span=np.array([[0, 1], [1, 2], [5, 9]], np.int32),
+                             o_span=np.array([[0, 1], [0, 2], [100, 101]], np.int32))
+    head, w = head_for(FULL)
+    gpu = run_gpu(head, bt)
+    ref = run_oracle(w, FULL, bt)
+    np.testing.assert_array_equal(gpu["probs"], np.ones(3, np.float32))
+    compare(gpu, ref, bt)
+
+
+# ------------------------------------------------------------ invariances
+
+def test_padding_invariance_bitwise():
+    a = synth.make_batch(ragged_spec(B=2, length_range=(400, 1300)), seed=9)
+    b = synth.make_batch(ragged_spec(B=2, length_range=(400, 1300)), seed=9, lpad=int(a.Lpad) + 333)
+    head, _ = head_for(FULL)
+    ga, gb = run_gpu(head, a), run_gpu(head, b)
+    for k in ga:
+        np.testing.assert_array_equal(ga[k], gb[k])
+
+
+def test_batch_invariance_bitwise():
+    bt = synth.make_batch(ragged_spec(B=3, length_range=(400, 1500)), seed=10)
+    head, _ = head_for(FULL)
+    full = run_gpu(head, bt)
+    b = 1
+    qs = np.nonzero(bt.q_rec == b)[0]
+    lo, hi = bt.q_opt_off[qs[0]], bt.q_opt_off[qs[-1] + 1]
+    one = dataclasses.replace(bt, B=1, lengths=bt.lengths[b:b + 1], q_rec=np.zeros(len(qs), np.int32),
+                              q_type=bt.q_type[qs], q_span=bt.q_span[qs],
+                              q_opt_off=(bt.q_opt_off[qs[0]:qs[-1] + 2] - lo).astype(np.int32),
+                              o_span=bt.o_span[lo:hi], token_ids=bt.token_ids[b:b + 1],
+                              hidden=bt.hidden[b:b + 1])
+    alone = run_gpu(head, one)
+    np.testing.assert_array_equal(alone["logits"], full["logits"][lo:hi])
+    np.testing.assert_array_equal(alone["q_argmax"], full["q_argmax"][qs])
+
+
+def test_repeat_calls_are_deterministic():
+    bt = synth.make_batch(ragged_spec(B=2, length_range=(500, 1100)), seed=13)
+    head, _ = head_for(FULL)
+    inputs = device_inputs(bt, FULL.vocab)
+    a = run_gpu(head, bt, inputs=inputs)
+    b = run_gpu(head, bt, inputs=inputs)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])

@@ -19,7 +19,7 @@ import synth
 from oracle.clef_head import HeadParams, linear
 from synth import BatchSpec, HeadShape
 
-torch.set_default_dtype(torch.float64)
+F64 = dict(dtype=torch.float64)
 
 TINY = HeadShape(H=48, D=32, heads=4, F=64, vocab=500)
 
@@ -144,7 +144,7 @@ def test_raw_span_sums_integer_bruteforce():
 
 def _mha_ref(qx, mem, Wq, bq, Wk, bk, Wv, bv, Wo, bo, heads):
     D, H = Wq.shape[0], Wk.shape[1]
-    mha = torch.nn.MultiheadAttention(D, heads, bias=True, kdim=H, vdim=H, batch_first=True)
+    mha = torch.nn.MultiheadAttention(D, heads, bias=True, kdim=H, vdim=H, batch_first=True, **F64)
     with torch.no_grad():
         mha.q_proj_weight.copy_(T(Wq))
         mha.k_proj_weight.copy_(T(Wk))
@@ -187,9 +187,9 @@ def test_routing_layer_matches_torch_modules():
     got = oracle.routing_layer(o, mem, 1, p)
     q = "route.1."
     D = TINY.D
-    ln1 = torch.nn.LayerNorm(D, eps=1e-5)
-    ln2 = torch.nn.LayerNorm(D, eps=1e-5)
-    ffn = torch.nn.Sequential(torch.nn.Linear(D, TINY.F), torch.nn.GELU(), torch.nn.Linear(TINY.F, D))
+    ln1 = torch.nn.LayerNorm(D, eps=1e-5, **F64)
+    ln2 = torch.nn.LayerNorm(D, eps=1e-5, **F64)
+    ffn = torch.nn.Sequential(torch.nn.Linear(D, TINY.F, **F64), torch.nn.GELU(), torch.nn.Linear(TINY.F, D, **F64))
     with torch.no_grad():
         ln1.weight.copy_(T(p[q + "attn_ln.weight"]))
         ln1.bias.copy_(T(p[q + "attn_ln.bias"]))
@@ -214,7 +214,7 @@ def test_joint_layer_matches_torch_encoder_layer(n):
     D = TINY.D
     layer = torch.nn.TransformerEncoderLayer(D, TINY.heads, dim_feedforward=TINY.F, dropout=0.0,
                                              activation="gelu", layer_norm_eps=1e-5,
-                                             batch_first=True, norm_first=True)
+                                             batch_first=True, norm_first=True, **F64)
     with torch.no_grad():
         layer.self_attn.in_proj_weight.copy_(T(p[q + "qkv.weight"]))
         layer.self_attn.in_proj_bias.copy_(T(p[q + "qkv.bias"]))
@@ -245,7 +245,7 @@ def test_field_aggregate_uniform_pool_and_terms():
     pz = HeadParams(t, p.heads, p.n_route, p.n_joint)
     u, oh, g = rng.normal(size=TINY.H), rng.normal(size=(4, TINY.D)), rng.normal(size=TINY.H)
     got = oracle.field_aggregate(u, oh, g, 2, pz)
-    lin = torch.nn.Linear(TINY.H, TINY.D, bias=False)
+    lin = torch.nn.Linear(TINY.H, TINY.D, bias=False, **F64)
     with torch.no_grad():
         lin.weight.copy_(T(p["field.question.weight"]))
         a = lin(T(u)).numpy()
@@ -286,7 +286,7 @@ def test_scorer_open_gate_matches_torch_terms():
     x, u, g = rng.normal(size=(4, TINY.H)), rng.normal(size=TINY.H), rng.normal(size=TINY.H)
     f, oh = rng.normal(size=TINY.D), rng.normal(size=(4, TINY.D))
     D = TINY.D
-    mlp = torch.nn.Sequential(torch.nn.Linear(4 * D, D), torch.nn.GELU(), torch.nn.Linear(D, 1))
+    mlp = torch.nn.Sequential(torch.nn.Linear(4 * D, D, **F64), torch.nn.GELU(), torch.nn.Linear(D, 1, **F64))
     with torch.no_grad():
         mlp[0].weight.copy_(T(p["scorer.mlp1.weight"]))
         mlp[0].bias.copy_(T(p["scorer.mlp1.bias"]))
