@@ -176,7 +176,9 @@ CLEF_API int clef_head_forward(const clef_config* cfg, const void* const* weight
                       const clef_debug_outputs* debug, void* stream);
 
 /* Waits for `stream`, then reads and clears the device-side status word kept at the
- * start of `workspace`: CLEF_OK, CLEF_ERR_DEVICE_BOUNDS or CLEF_ERR_DEVICE_TIMEOUT. */
+ * start of `workspace`: CLEF_OK, CLEF_ERR_DEVICE_BOUNDS or CLEF_ERR_DEVICE_TIMEOUT.
+ * Every clef_head_forward / clef_span_sums call clears that word when it starts, so
+ * the status covers the latest call on the workspace. */
 CLEF_API int clef_device_status(void* workspace, void* stream);
 
 /* Index check of the pooling step ("clef-4bit JointSchemaHead walkthrough" section 3

@@ -1,0 +1,276 @@
+// Routing cross-attention of the EvidenceRoutingLayers ("clef-4bit JointSchemaHead
+// walkthrough" section 3 step 2: every option is a query over the whole memory),
+// split over the memory length (flash-decoding style) and merged afterwards.
+//
+// Work item = (record chunk of kAttnChunk memory rows, head, block of 64 option
+// queries).  A producer warp streams 64-row K and V tiles of the chunk with TMA
+// (128-byte swizzle) through a 4-stage mbarrier ring; four consumer warps each own
+// 16 queries and run QK^T and PV on mma.sync bf16 tensor cores with an fp32
+// online softmax in the exp2 domain.  Keys at or past the chunk end are masked.
+// Every (option, head, chunk) leaves (running max, running sum, unnormalised
+// accumulator); the merge kernel rescales and sums the chunks of a record.
+// Every mbarrier wait is bounded; on a timeout the CTA flags it and returns.
+#include <mutex>
+
+#include "common.cuh"
+#include "head_kernels.h"
+#include "kernels.h"
+
+namespace clef {
+
+namespace {
+
+constexpr int kKT = 64;                     // keys per tile
+constexpr int kStages = 4;
+constexpr int kQRows = 64;                  // option queries per CTA (4 consumer warps x 16)
+constexpr int kTileBytes = kKT * 128;       // [64 rows][64 bf16]
+constexpr int kQBytes = kQRows * 128;
+constexpr int kSmem = kQBytes + kStages * 2 * kTileBytes + 1024 + 128;
+constexpr int kThreads = 160;               // 4 consumer warps + 1 producer warp
+
+// byte offset of 16-byte chunk `chunk` of row `row` in a tile written by TMA with the
+// 128-byte swizzle (chunk index XOR row mod 8, tile base 1024-byte aligned)
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 3)
+    route_attn_partial_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                              const RouteAttnArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + kQBytes;  // stage s: K at s * 2 * kTileBytes, V right after
+    uint64_t* full = reinterpret_cast<uint64_t*>(sKV + kStages * 2 * kTileBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* qbar = empty + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(qbar + 1);
+
+    const int cx = blockIdx.x, h = blockIdx.y, qp = blockIdx.z;
+    const int b = a.chunk_rec[cx], kc = a.chunk_idx[cx];
+    const int o_base = a.rec_o_off[b];
+    const int O_b = a.rec_o_off[b + 1] - o_base;
+    if (qp * kQRows >= O_b) return;  // this record has fewer query blocks
+    const int L = a.lengths[b];
+    const int t0 = kc * kAttnChunk;
+    const int t1 = min(t0 + kAttnChunk, L);
+    const int n_tiles = (t1 - t0 + kKT - 1) / kKT;
+    const int kv_row0 = a.rec_row_off[b] + t0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        mbar_init(qbar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 4) {  // producer
+        if (lane == 0) {
+            prefetch_tensormap(&tmQ);
+            prefetch_tensormap(&tmKV);
+            mbar_arrive_expect_tx(qbar, kQBytes);
+            tma_load_2d(sQ, &tmQ, h * 64, o_base + qp * kQRows, qbar);
+            uint32_t armed[kStages] = {0, 0, 0, 0};
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int kt = 0; kt < n_tiles; ++kt) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.flags)) break;
+                mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                uint8_t* dst = sKV + stage * 2 * kTileBytes;
+                const int row = kv_row0 + kt * kKT;
+                tma_load_2d(dst, &tmKV, a.k_col + h * 64, row, &full[stage]);
+                tma_load_2d(dst + kTileBytes, &tmKV, a.v_col + h * 64, row, &full[stage]);
+                ++armed[stage];
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // every copy this thread started lands before the CTA can exit
+            mbar_wait_bounded(qbar, 0, nullptr, nullptr);
+            for (int s = 0; s < kStages; ++s)
+                if (armed[s]) mbar_wait_bounded(&full[s], (armed[s] - 1) & 1u, nullptr, nullptr);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int g = lane >> 2, tq = lane & 3;
+    const int wrow0 = warp * 16;
+    const bool active = qp * kQRows + wrow0 < O_b;
+    const float sl2 = a.scale_log2;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(qbar, 0, abort_flag, a.flags) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    uint32_t qa[4][4];
+    if (ok && active) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            ldmatrix_x4(qa[ks], smem_u32(sQ) + swz(wrow0 + (lane & 15), ks * 2 + (lane >> 4)));
+    }
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int kt = 0; kt < n_tiles && ok; ++kt) {
+        if (lane == 0) ok = mbar_wait_bounded(&full[stage], phase, abort_flag, a.flags) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (active) {
+            const uint32_t kb = smem_u32(sKV + stage * 2 * kTileBytes);
+            const uint32_t vb = kb + kTileBytes;
+            float s[8][4];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                for (int jp = 0; jp < 4; ++jp) {  // pairs of 8-key n-tiles
+                    uint32_t kr[4];
+                    ldmatrix_x4(kr, kb + swz(jp * 16 + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
+                    mma_bf16_16816(s[2 * jp], qa[ks], kr[0], kr[1]);
+                    mma_bf16_16816(s[2 * jp + 1], qa[ks], kr[2], kr[3]);
+                }
+            }
+            const int kbase = t0 + kt * kKT;
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int key = kbase + j * 8 + tq * 2 + (c & 1);
+                    const float v = key < t1 ? s[j][c] * sl2 : -INFINITY;
+                    s[j][c] = v;
+                    mx[c >> 1] = fmaxf(mx[c >> 1], v);
+                }
+            }
+            float corr[2], ps[2] = {0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                const float mn = fmaxf(m_r[r], mx[r]);
+                corr[r] = exp2f(m_r[r] - mn);
+                m_r[r] = mn;
+            }
+            uint32_t pa[4][4];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float p0 = exp2f(s[j][0] - m_r[0]), p1 = exp2f(s[j][1] - m_r[0]);
+                const float p2 = exp2f(s[j][2] - m_r[1]), p3 = exp2f(s[j][3] - m_r[1]);
+                ps[0] += p0 + p1;
+                ps[1] += p2 + p3;
+                pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
+                pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) l_r[r] = l_r[r] * corr[r] + ps[r];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                acc[j][0] *= corr[0]; acc[j][1] *= corr[0];
+                acc[j][2] *= corr[1]; acc[j][3] *= corr[1];
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                for (int dp = 0; dp < 4; ++dp) {  // pairs of 8-dim n-tiles
+                    uint32_t vr[4];
+                    ldmatrix_x4_trans(vr, vb + swz(ks * 16 + (lane & 15), dp * 2 + (lane >> 4)));
+                    mma_bf16_16816(acc[2 * dp], pa[ks], vr[0], vr[1]);
+                    mma_bf16_16816(acc[2 * dp + 1], pa[ks], vr[2], vr[3]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (!ok || !active) return;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
+        l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
+    }
+    const int64_t part_base = a.rec_part_off[b] + (int64_t(kc) * a.heads + h) * O_b;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int o = qp * kQRows + wrow0 + g + r * 8;
+        if (o < O_b) {
+            const int64_t pi = part_base + o;
+            if (tq == 0) {
+                a.pm[pi] = m_r[r];
+                a.pl[pi] = l_r[r];
+            }
+            float* dst = a.pacc + pi * 64;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float2*>(dst + j * 8 + tq * 2) = make_float2(acc[j][2 * r], acc[j][2 * r + 1]);
+        }
+    }
+}
+
+// Merge of the split-L partials of one (option, head): one warp, 2 dims per lane.
+__global__ void __launch_bounds__(256) route_attn_merge_kernel(const RouteAttnArgs a, int O) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + warp;
+    if (item >= O * a.heads) return;
+    const int o = item / a.heads, h = item % a.heads;
+    const int b = a.o_rec[o];
+    const int o_base = a.rec_o_off[b];
+    const int O_b = a.rec_o_off[b + 1] - o_base;
+    const int nch = (a.lengths[b] + kAttnChunk - 1) / kAttnChunk;
+    float M = -INFINITY;
+    for (int k = 0; k < nch; ++k)
+        M = fmaxf(M, a.pm[a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base)]);
+    float Ls = 0.f, x0 = 0.f, x1 = 0.f;
+    for (int k = 0; k < nch; ++k) {
+        const int64_t pi = a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base);
+        const float w = exp2f(a.pm[pi] - M);
+        Ls += a.pl[pi] * w;
+        const float2 v = *reinterpret_cast<const float2*>(a.pacc + pi * 64 + lane * 2);
+        x0 += v.x * w;
+        x1 += v.y * w;
+    }
+    const float inv = 1.0f / Ls;
+    *reinterpret_cast<uint32_t*>(a.out + int64_t(o) * a.ldo + h * 64 + lane * 2) = pack_bf16(x0 * inv, x1 * inv);
+}
+
+cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, int O, int max_rec_options,
+                                      cudaStream_t s) {
+    if (n_chunks <= 0 || O <= 0) return cudaSuccess;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(route_attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap tq, tkv;
+    if (!make_tma_2d_bf16(&tq, a.q, uint64_t(a.heads) * 64, uint64_t(O), uint64_t(a.ldq), 64))
+        return cudaErrorInvalidValue;
+    if (!make_tma_2d_bf16(&tkv, a.kv, uint64_t(a.ldkv), uint64_t(a.kv_rows), uint64_t(a.ldkv), 64))
+        return cudaErrorInvalidValue;
+    const int qblocks = (max_rec_options + kQRows - 1) / kQRows;
+    route_attn_partial_kernel<<<dim3(n_chunks, a.heads, qblocks), kThreads, kSmem, s>>>(tq, tkv, a);
+    return counted(cudaGetLastError());
+}
+
+cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s) {
+    if (O <= 0) return cudaSuccess;
+    route_attn_merge_kernel<<<(O * a.heads + 7) / 8, 256, 0, s>>>(a, O);
+    return counted(cudaGetLastError());
+}
+
+}  // namespace clef

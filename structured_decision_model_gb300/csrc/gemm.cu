@@ -13,6 +13,7 @@
 // visited N-fastest so that CTAs working at the same time share A tiles in L2.
 // Every mbarrier wait is bounded: on a timeout the CTA sets the timeout flag,
 // waits (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
@@ -29,10 +30,26 @@ constexpr int kThreads = 192;
 
 struct GemmArgs {
     int n_mtiles, n_ntiles, kblocks;
+    int splits, kb_per_split;      // split-K: each output tile's K range cut into `splits` parts
     const int32_t* a_row_of_mtile;
     GemmEpilogue epi;
+    float* partial;                // [tiles * splits][BM][BN] fp32 partial tiles (splits > 1)
+    int* counters;                 // [tiles][4] arrival counters, zero between launches (splits > 1)
     int* dev_flags;
 };
+
+// Tile t of the persistent walk: split fastest, then N, then M.
+struct TileId {
+    int mt, nt, sp, out;  // out = output tile index (mt * n_ntiles + nt)
+};
+__device__ __forceinline__ TileId decode_tile(const GemmArgs& a, int t) {
+    TileId id;
+    id.sp = t % a.splits;
+    id.out = t / a.splits;
+    id.mt = id.out / a.n_ntiles;
+    id.nt = id.out % a.n_ntiles;
+    return id;
+}
 
 template <int BN>
 struct GemmCfg {
@@ -50,8 +67,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
     if (e.kind == EPI_KV_LNFOLD) {
         const float mu = e.row_mu[m], rs = e.row_rstd[m];
+        // rstd == 0 marks a row of a record's round-up slack: stored as zeros, so that
+        // whatever the padding held never reaches attention as a non-finite value
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = rs * (v[j] - mu * e.col_c[n0 + j]) + e.bias_f32[n0 + j];
+        for (int j = 0; j < 16; ++j) v[j] = rs == 0.f ? 0.f : rs * (v[j] - mu * e.col_c[n0 + j]) + e.bias_f32[n0 + j];
     } else {
         if (e.bias_bf16) {
             const uint4* bp = reinterpret_cast<const uint4*>(e.bias_bf16 + n0);
@@ -145,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_tiles = args.n_mtiles * args.n_ntiles;
+    const int n_tiles = args.n_mtiles * args.n_ntiles * args.splits;
     const int kblocks = args.kblocks;
 
     if (warp == 0) {
@@ -156,10 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const int mt = tile / args.n_ntiles, nt = tile % args.n_ntiles;
-                const int a_row = args.a_row_of_mtile ? args.a_row_of_mtile[mt] : mt * BM;
-                const int b_row = nt * BN;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                const TileId id = decode_tile(args, tile);
+                const int a_row = args.a_row_of_mtile ? args.a_row_of_mtile[id.mt] : id.mt * BM;
+                const int b_row = id.nt * BN;
+                const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.dev_flags)) {
                         ok = false;
                         break;
@@ -193,7 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait_bounded(&tempty[acc], (use & 1u) ^ 1u, abort_flag, args.dev_flags)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                const TileId id = decode_tile(args, tile);
+                const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.dev_flags)) {
                         ok = false;
                         break;
@@ -204,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
-                                    (kb | k) != 0);
+                                    (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     tc_commit(&empty[stage]);
                     if (++stage == C::STAGES) {
@@ -231,18 +253,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int mt = tile / args.n_ntiles, nt = tile % args.n_ntiles;
-            const int m = mt * BM + r_in_tile;
+            const TileId id = decode_tile(args, tile);
+            const int m = id.mt * BM + r_in_tile;
             const bool store = m < args.epi.M;
+            if (args.splits == 1) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 16; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem_base + uint32_t(acc * BN + c * 16) + (uint32_t(quarter * 32) << 16), r);
+                    tmem_ld_wait();
+                    if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r);
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+                continue;
+            }
+            // split-K: park this split's fp32 rows, count arrivals per (output tile, warp
+            // quarter); the warp whose arrival completes the count sums every split in
+            // split order (deterministic) and runs the epilogue for its 32 rows.  No
+            // warp waits for another.
+            float* mine = args.partial + (int64_t(id.out) * args.splits + id.sp) * (BM * BN) + r_in_tile * BN;
 #pragma unroll 1
             for (int c = 0; c < BN / 16; ++c) {
                 uint32_t r[16];
                 tmem_ld16(tmem_base + uint32_t(acc * BN + c * 16) + (uint32_t(quarter * 32) << 16), r);
                 tmem_ld_wait();
-                if (store) epilogue_chunk<BN>(args.epi, m, nt * BN + c * 16, r);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    __stcg(reinterpret_cast<float4*>(mine + c * 16) + q,
+                           make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            mbar_arrive(&tempty[acc]);  // TMEM is free again; the rest works from global memory
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = atomicAdd(args.counters + id.out * 4 + quarter, 1) == args.splits - 1;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                const float* base = args.partial + int64_t(id.out) * args.splits * (BM * BN) + r_in_tile * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 16; ++c) {
+                    float v[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                    for (int sp = 0; sp < args.splits; ++sp) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 w =
+                                __ldcg(reinterpret_cast<const float4*>(base + int64_t(sp) * (BM * BN) + c * 16) + q);
+                            v[4 * q] += w.x; v[4 * q + 1] += w.y; v[4 * q + 2] += w.z; v[4 * q + 3] += w.w;
+                        }
+                    }
+                    uint32_t r[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(v[j]);
+                    if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r);
+                }
+                if (lane == 0) args.counters[id.out * 4 + quarter] = 0;  // ready for the next launch
+            }
         }
     }
     __syncthreads();
@@ -272,8 +343,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
-              uint32_t box_rows) {
+}  // namespace
+
+bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
+                      uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, rows};
@@ -285,6 +358,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
 template <int BN>
 cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s) {
     using C = GemmCfg<BN>;
@@ -295,17 +370,32 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, p.A, uint64_t(p.K), uint64_t(p.a_rows), uint64_t(p.lda), BM)) return cudaErrorInvalidValue;
-    if (!make_map(&tb, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN)) return cudaErrorInvalidValue;
+    if (!make_tma_2d_bf16(&ta, p.A, uint64_t(p.K), uint64_t(p.a_rows), uint64_t(p.lda), BM)) return cudaErrorInvalidValue;
+    if (!make_tma_2d_bf16(&tb, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN)) return cudaErrorInvalidValue;
     GemmArgs a;
     a.n_mtiles = p.n_mtiles;
     a.n_ntiles = p.N / BN;
     a.kblocks = p.K / BK;
+    a.splits = 1;
+    a.kb_per_split = a.kblocks;
     a.a_row_of_mtile = p.a_row_of_mtile;
     a.epi = e;
+    a.partial = p.split_partial;
+    a.counters = p.split_counters;
     a.dev_flags = flags;
-    const int tiles = a.n_mtiles * a.n_ntiles;
-    const int grid = tiles < num_sms() ? tiles : num_sms();
+    const int sms = num_sms();
+    const int out_tiles = a.n_mtiles * a.n_ntiles;
+    if (p.split_partial && p.split_counters && out_tiles < sms && a.kblocks >= 8) {
+        // cut K so that about one wave of CTAs is busy, at least 4 K blocks per split
+        int want = std::min(std::min(sms / out_tiles, a.kblocks / 4), kMaxSplits);
+        want = std::min(want, kSplitSlots / out_tiles);
+        if (want > 1) {
+            a.kb_per_split = (a.kblocks + want - 1) / want;
+            a.splits = (a.kblocks + a.kb_per_split - 1) / a.kb_per_split;
+        }
+    }
+    const int tiles = out_tiles * a.splits;
+    const int grid = tiles < sms ? tiles : sms;
     gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, s>>>(ta, tb, a);
     return counted(cudaGetLastError());
 }

@@ -210,221 +210,6 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const float* __restrict
 }
 
 // =====================================================================
-// Routing cross-attention, split over the memory length ("clef-4bit JointSchemaHead
-// walkthrough" section 3 step 2: every option queries the whole memory).
-// One CTA per (record chunk of kAttnChunk keys, head).  8 warps take 16 option
-// queries each (128 per pass; more passes for larger records).  K/V tiles of 64
-// keys stream through a double-buffered, XOR-swizzled shared-memory ring with
-// cp.async; QK^T and PV run on mma.sync bf16 tensor cores with an online softmax
-// (exp2 domain).  Keys at or past the chunk end are zero-filled and masked.
-// Each (option, head, chunk) leaves (max, sum, unnormalised accumulator).
-// =====================================================================
-namespace {
-constexpr int kKT = 64;  // keys per tile
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a [rows][64 bf16] tile
-    return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-}  // namespace
-
-__global__ void __launch_bounds__(256) route_attn_partial_kernel(RouteAttnArgs a) {
-    __shared__ __align__(128) uint8_t sQ[128 * 128];
-    __shared__ __align__(128) uint8_t sK[2][kKT * 128];
-    __shared__ __align__(128) uint8_t sV[2][kKT * 128];
-
-    const int cx = blockIdx.x, h = blockIdx.y;
-    const int b = a.chunk_rec[cx], kc = a.chunk_idx[cx];
-    const int L = a.lengths[b];
-    const int t0 = kc * kAttnChunk;
-    const int t1 = min(t0 + kAttnChunk, L);
-    const int n_tiles = (t1 - t0 + kKT - 1) / kKT;
-    const int o_base = a.rec_o_off[b];
-    const int O_b = a.rec_o_off[b + 1] - o_base;
-    const int64_t kv_row0 = a.rec_row_off[b];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const float sl2 = a.scale_log2;
-    const int64_t part_base = a.rec_part_off[b] + (int64_t(kc) * a.heads + h) * O_b;
-
-    auto load_kv = [&](int tile, int buf) {
-        // 64 rows x 8 chunks for K and for V: 1024 16-byte copies, 4 per thread
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int id = threadIdx.x + i * 256;
-            const int which = id >> 9;  // 0 = K, 1 = V
-            const int row = (id >> 3) & 63, ch = id & 7;
-            const int t = t0 + tile * kKT + row;
-            const bool valid = t < t1;
-            const uint16_t* src = a.kv + (kv_row0 + (valid ? t : t0)) * a.ldkv + (which ? a.v_col : a.k_col) +
-                                  h * 64 + ch * 8;
-            uint8_t* dst = (which ? sV[buf] : sK[buf]) + swz(row, ch);
-            cp_async16(dst, src, valid);
-        }
-    };
-
-    for (int qp = 0; qp * 128 < O_b; ++qp) {
-        // Q tile: 128 rows x 8 chunks
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int id = threadIdx.x + i * 256;
-            const int row = id >> 3, ch = id & 7;
-            const int o = qp * 128 + row;
-            const bool valid = o < O_b;
-            const uint16_t* src = a.q + int64_t(o_base + (valid ? o : 0)) * a.ldq + h * 64 + ch * 8;
-            cp_async16(sQ + swz(row, ch), src, valid);
-        }
-        load_kv(0, 0);
-        cp_async_commit();
-
-        const int wrow0 = warp * 16;
-        const bool active = qp * 128 + wrow0 < O_b;
-        uint32_t qa[4][4];
-        float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-        float acc[8][4];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-        for (int kt = 0; kt < n_tiles; ++kt) {
-            if (kt + 1 < n_tiles) load_kv(kt + 1, (kt + 1) & 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-            __syncthreads();
-            if (kt == 0 && active) {
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const int row = wrow0 + (lane & 15);
-                    const int ch = ks * 2 + (lane >> 4);
-                    ldmatrix_x4(qa[ks], smem_u32(sQ) + swz(row, ch));
-                }
-            }
-            if (active) {
-                const uint8_t* kb = sK[kt & 1];
-                const uint8_t* vb = sV[kt & 1];
-                float s[8][4];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-                    for (int jp = 0; jp < 4; ++jp) {  // pairs of 8-key n-tiles
-                        uint32_t kr[4];
-                        const int key = jp * 16 + (lane & 7) + ((lane >> 4) << 3);
-                        const int ch = ks * 2 + ((lane >> 3) & 1);
-                        ldmatrix_x4(kr, smem_u32(kb) + swz(key, ch));
-                        mma_bf16_16816(s[2 * jp], qa[ks], kr[0], kr[1]);
-                        mma_bf16_16816(s[2 * jp + 1], qa[ks], kr[2], kr[3]);
-                    }
-                }
-                // scale, mask, online softmax
-                const int kbase = t0 + kt * kKT;
-                float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int key = kbase + j * 8 + tq * 2 + (c & 1);
-                        const float v = key < t1 ? s[j][c] * sl2 : -INFINITY;
-                        s[j][c] = v;
-                        mx[c >> 1] = fmaxf(mx[c >> 1], v);
-                    }
-                }
-                float corr[2], ps[2] = {0.f, 0.f};
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                    const float mn = fmaxf(m_r[r], mx[r]);
-                    corr[r] = exp2f(m_r[r] - mn);
-                    m_r[r] = mn;
-                }
-                uint32_t pa[4][4];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float p0 = exp2f(s[j][0] - m_r[0]), p1 = exp2f(s[j][1] - m_r[0]);
-                    const float p2 = exp2f(s[j][2] - m_r[1]), p3 = exp2f(s[j][3] - m_r[1]);
-                    ps[0] += p0 + p1;
-                    ps[1] += p2 + p3;
-                    pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
-                    pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
-                }
-#pragma unroll
-                for (int r = 0; r < 2; ++r) l_r[r] = l_r[r] * corr[r] + ps[r];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    acc[j][0] *= corr[0]; acc[j][1] *= corr[0];
-                    acc[j][2] *= corr[1]; acc[j][3] *= corr[1];
-                }
-                // P (16 x 64 keys) * V (64 keys x 64 dims)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    // A fragment order: (row g, keys lo), (row g+8, keys lo), (row g, keys hi), (row g+8, keys hi)
-                    uint32_t af[4] = {pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3]};
-#pragma unroll
-                    for (int dp = 0; dp < 4; ++dp) {  // pairs of 8-dim n-tiles
-                        uint32_t vr[4];
-                        const int key = ks * 16 + (lane & 15);
-                        const int ch = dp * 2 + (lane >> 4);
-                        ldmatrix_x4_trans(vr, smem_u32(vb) + swz(key, ch));
-                        mma_bf16_16816(acc[2 * dp], af, vr[0], vr[1]);
-                        mma_bf16_16816(acc[2 * dp + 1], af, vr[2], vr[3]);
-                    }
-                }
-            }
-            __syncthreads();
-        }
-        // per-row totals across the quad, then write the partials
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-        }
-        if (active) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int o = qp * 128 + wrow0 + g + r * 8;
-                if (o < O_b) {
-                    const int64_t pi = part_base + o;
-                    if (tq == 0) {
-                        a.pm[pi] = m_r[r];
-                        a.pl[pi] = l_r[r];
-                    }
-                    float* dst = a.pacc + pi * 64;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<float2*>(dst + j * 8 + tq * 2) = make_float2(acc[j][2 * r], acc[j][2 * r + 1]);
-                }
-            }
-        }
-        __syncthreads();
-    }
-}
-
-// Merge of the split-L partials of one (option, head): one warp, 2 dims per lane.
-__global__ void __launch_bounds__(256) route_attn_merge_kernel(RouteAttnArgs a, int O) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int item = blockIdx.x * 8 + warp;
-    if (item >= O * a.heads) return;
-    const int o = item / a.heads, h = item % a.heads;
-    const int b = a.o_rec[o];
-    const int o_base = a.rec_o_off[b];
-    const int O_b = a.rec_o_off[b + 1] - o_base;
-    const int nch = (a.lengths[b] + kAttnChunk - 1) / kAttnChunk;
-    float M = -INFINITY;
-    for (int k = 0; k < nch; ++k)
-        M = fmaxf(M, a.pm[a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base)]);
-    float Ls = 0.f, x0 = 0.f, x1 = 0.f;
-    for (int k = 0; k < nch; ++k) {
-        const int64_t pi = a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base);
-        const float w = exp2f(a.pm[pi] - M);
-        Ls += a.pl[pi] * w;
-        const float2 v = *reinterpret_cast<const float2*>(a.pacc + pi * 64 + lane * 2);
-        x0 += v.x * w;
-        x1 += v.y * w;
-    }
-    const float inv = 1.0f / Ls;
-    *reinterpret_cast<uint32_t*>(a.out + int64_t(o) * a.ldo + h * 64 + lane * 2) = pack_bf16(x0 * inv, x1 * inv);
-}
-
-// =====================================================================
 // Field aggregation, summary part ("clef-4bit JointSchemaHead walkthrough" section 3
 // step 3, option-weighted summary): alpha = softmax_j(w_a . o_hat_j + b_a) over
 // the question's options; summary = sum_j alpha_j o_hat_j, written as bf16 into
@@ -648,6 +433,17 @@ __global__ void __launch_bounds__(256) fold_kv_kernel(FoldArgs a) {
     }
 }
 
+// Launch-plan upload: the host's plan tables travel as kernel parameters (copied by
+// the launch itself, so no host buffer has to outlive the call and nothing waits).
+struct PlanChunk {
+    int32_t n;
+    int32_t data[kPlanChunkInts];
+};
+
+__global__ void __launch_bounds__(256) plan_upload_kernel(int32_t* __restrict__ dst, const PlanChunk c) {
+    for (int i = threadIdx.x; i < c.n; i += blockDim.x) dst[i] = c.data[i];
+}
+
 // dst[r][col_off + c] = src[r][c] for a [rows][cols] bf16 block (16-byte units).
 __global__ void __launch_bounds__(256) copy_cols_kernel(uint16_t* __restrict__ dst, int64_t ld_dst, int col_off,
                                                        const uint16_t* __restrict__ src, int64_t ld_src, int rows,
@@ -685,18 +481,6 @@ cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w
     return counted(cudaGetLastError());
 }
 
-cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, cudaStream_t s) {
-    if (n_chunks <= 0) return cudaSuccess;
-    route_attn_partial_kernel<<<dim3(n_chunks, a.heads), 256, 0, s>>>(a);
-    return counted(cudaGetLastError());
-}
-
-cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s) {
-    if (O <= 0) return cudaSuccess;
-    route_attn_merge_kernel<<<(O * a.heads + 7) / 8, 256, 0, s>>>(a, O);
-    return counted(cudaGetLastError());
-}
-
 cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,
                               const uint16_t* b_a, uint16_t* out, int64_t ldo, int col_off, cudaStream_t s) {
     if (Q <= 0) return cudaSuccess;
@@ -723,6 +507,18 @@ cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s) {
     if (Q <= 0) return cudaSuccess;
     score_softmax_kernel<<<Q, 256, 0, s>>>(a);
     return counted(cudaGetLastError());
+}
+
+cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaStream_t s) {
+    PlanChunk c;
+    for (size_t off = 0; off < n; off += kPlanChunkInts) {
+        c.n = int32_t(n - off < size_t(kPlanChunkInts) ? n - off : size_t(kPlanChunkInts));
+        for (int i = 0; i < c.n; ++i) c.data[i] = src[off + i];
+        plan_upload_kernel<<<1, 256, 0, s>>>(dst + off, c);
+        const cudaError_t e = counted(cudaGetLastError());
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_fold_kv(const FoldArgs& a, int rows, cudaStream_t s) {

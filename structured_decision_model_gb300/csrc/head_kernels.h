@@ -9,6 +9,7 @@ namespace clef {
 constexpr int kAttnChunk = 1024;  // memory rows per split-L routing-attention work item
 constexpr int kMaxFields = 48;    // questions per record handled by the field self-attention kernel
 constexpr int kMaxOptions = 256;  // options per question
+constexpr int kPlanChunkInts = 4000;  // plan ints carried by one upload launch (16 KB of parameters)
 
 struct SpanPoolArgs {
     const uint16_t* hidden; int64_t row_stride; int Lpad; int H; int vocab;
@@ -32,6 +33,7 @@ struct SpanPoolArgs {
 struct RouteAttnArgs {
     const uint16_t* q; int64_t ldq;       // [O][D] bf16 queries
     const uint16_t* kv; int64_t ldkv;     // [R][ldkv] bf16 memory keys / values
+    int64_t kv_rows;                      // R
     int k_col, v_col;                     // column of this layer's K and V blocks
     int heads;
     float scale_log2;                     // log2(e) / sqrt(head dim)
@@ -41,6 +43,7 @@ struct RouteAttnArgs {
     const int32_t* o_rec;
     float* pm; float* pl; float* pacc;    // partials
     uint16_t* out; int64_t ldo;           // [O][D] bf16 merged output
+    int* flags;                           // device status word
 };
 
 struct ScoreArgs {
@@ -67,7 +70,8 @@ cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpa
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s);
 cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
                               uint16_t* out_bf16, float* out_f32, cudaStream_t s);
-cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, cudaStream_t s);
+cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, int O, int max_rec_options,
+                                      cudaStream_t s);
 cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s);
 cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,
                               const uint16_t* b_a, uint16_t* out, int64_t ldo, int col_off, cudaStream_t s);
@@ -77,6 +81,7 @@ cudaError_t launch_build_z(const float* f_hat, const float* o_hat, const int32_t
                            cudaStream_t s);
 cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s);
 cudaError_t launch_fold_kv(const FoldArgs& a, int rows, cudaStream_t s);
+cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaStream_t s);
 cudaError_t launch_copy_cols(uint16_t* dst, int64_t ld_dst, int col_off, const uint16_t* src, int64_t ld_src,
                              int rows, int cols, cudaStream_t s);
 

@@ -1,6 +1,7 @@
 // Host-side launchers of the head's kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,9 +52,22 @@ struct GemmProblem {
     int N = 0, K = 0;
     int n_mtiles = 0;                        // 128-row output tiles
     const int32_t* a_row_of_mtile = nullptr; // device [n_mtiles]: first A row of each tile (null: 128 * tile)
+    // split-K scratch (both null: no split).  Partial tiles: kSplitSlots x 128 x 256 fp32;
+    // counters: 4 x kSplitSlots ints that are zero before the launch (the kernel leaves them zero).
+    float* split_partial = nullptr;
+    int* split_counters = nullptr;
 };
 
+constexpr int kMaxSplits = 16;    // K parts per output tile
+constexpr int kSplitSlots = 160;  // output tiles x splits of one split-K launch, at most
+constexpr size_t kSplitPartialBytes = size_t(kSplitSlots) * 128 * 256 * 4;
+
 int num_sms();
+
+// 2-D TMA descriptor of a row-major bf16 matrix [rows][inner] (row stride in elements),
+// 64-element x box_rows box, 128-byte swizzle.  Returns false if the driver rejects it.
+bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
+                      uint32_t box_rows);
 cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_flags, cudaStream_t s,
                         int force_bn = 0);
 
