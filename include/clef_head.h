@@ -191,6 +191,41 @@ CLEF_API int clef_span_sums(const clef_config* cfg, const clef_schema* schema, c
                    const int32_t* token_ids, const uint16_t* lexical, float* q_sum, float* o_sum,
                    float* x_sum, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Largest scratch the allocation-free span-sum entry point below can use. */
+#define CLEF_SPAN_SUMS_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* clef_span_sums for callers that cannot allocate device memory.  The pages have
+ * no counterpart of this entry point; it exists for callers that must not call
+ * cudaMalloc themselves: code that runs inside another runtime's fixed device-memory
+ * pool, a plug-in that is handed only its input and output buffers, or code paths
+ * where a device allocation would stall or fail.  Such callers cannot provide the
+ * workspace clef_span_sums needs.
+ *   - The scratch (the launch plan of the batch and the device status word) lives in
+ *     one static device array of CLEF_SPAN_SUMS_NOALLOC_SCRATCH_BYTES (1 MiB) inside
+ *     the library.  Every GPU that loads the library holds that array until the
+ *     process exits.  A schema whose plan does not fit returns
+ *     CLEF_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The plan takes 28
+ *     bytes per question, 24 per option, 32 per record and 8 per 128 memory rows, so
+ *     1 MiB holds, for example, 2 000 questions and 20 000 options over 256 records
+ *     of 16 384 rows.
+ *   - The caller passes inputs and outputs exactly as for clef_span_sums, and gets
+ *     the same sums bit for bit.
+ *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - The plan reaches the array as kernel parameters of small upload kernels, so no
+ *     host buffer is pinned or kept.
+ *   - The first call on a device looks up the device address of the array with
+ *     cudaGetSymbolAddress, with that device current.  Make that first call before
+ *     any stream capture.
+ *   - The call waits for `stream` before it returns, so that it can return a
+ *     device-side index error (CLEF_ERR_DEVICE_BOUNDS) directly.
+ *   - Every call uses the same array.  The status word is cleared at the start of
+ *     each call and the plan is rewritten, so nothing of an earlier call leaks into
+ *     a later one; but two calls that overlap on the GPU (other host threads, other
+ *     streams) race on the array and must be serialised by the caller. */
+CLEF_API int clef_span_sums_noalloc(const clef_config* cfg, const clef_schema* schema, const uint16_t* hidden,
+                                    const int32_t* token_ids, const uint16_t* lexical, float* q_sum,
+                                    float* o_sum, float* x_sum, void* stream);
+
 /* The dense-contraction kernel of the head on its own (tcgen05 / TMEM, TMA-fed):
  *   C[m][n] = sum_k A[m][k] * B[n][k] (+ bias[n]),  fp32 out, m < M, n < N.
  * A bf16 [M][K] row stride lda, B bf16 [N][K] row stride ldb, bias fp32 [N] or NULL,

@@ -20,7 +20,7 @@ STATUS = {
 EXPORTED = [
     "clef_weight_count", "clef_prepared_size", "clef_prepare_weights", "clef_workspace_size",
     "clef_head_forward", "clef_device_status", "clef_span_sums", "clef_gemm_bf16",
-    "clef_kernel_launches", "clef_status_string",
+    "clef_kernel_launches", "clef_status_string", "clef_span_sums_noalloc",
 ]
 
 _i32, _i64, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
@@ -71,6 +71,8 @@ def load():
     lib.clef_span_sums.argtypes = [ctypes.POINTER(ClefConfig), ctypes.POINTER(ClefSchema), _vp, _vp, _vp, _vp, _vp,
                                    _vp, _vp, _sz, _vp]
     lib.clef_gemm_bf16.argtypes = [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp]
+    lib.clef_span_sums_noalloc.argtypes = [ctypes.POINTER(ClefConfig), ctypes.POINTER(ClefSchema), _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _vp]
     lib.clef_kernel_launches.argtypes = []
     lib.clef_kernel_launches.restype = ctypes.c_uint64
     lib.clef_status_string.argtypes = [ctypes.c_int]
@@ -161,6 +163,13 @@ def clef_span_sums(cfg, schema: Schema, hidden_ptr, token_ids_ptr, lexical_ptr, 
     _check(load().clef_span_sums(ctypes.byref(cfg), ctypes.byref(schema.struct), hidden_ptr, token_ids_ptr,
                                  lexical_ptr, q_sum_ptr, o_sum_ptr, x_sum_ptr, workspace_ptr, workspace_bytes,
                                  stream), "clef_span_sums")
+
+
+def clef_span_sums_noalloc(cfg, schema: Schema, hidden_ptr, token_ids_ptr, lexical_ptr, q_sum_ptr, o_sum_ptr,
+                           x_sum_ptr, stream=0):
+    """Status of the allocation-free span sums (the call waits for ``stream``)."""
+    return load().clef_span_sums_noalloc(ctypes.byref(cfg), ctypes.byref(schema.struct), hidden_ptr,
+                                         token_ids_ptr, lexical_ptr, q_sum_ptr, o_sum_ptr, x_sum_ptr, stream)
 
 
 def clef_gemm_bf16(A_ptr, lda, B_ptr, ldb, bias_ptr, C_ptr, ldc, M, N, K, flags_ptr, stream=0):

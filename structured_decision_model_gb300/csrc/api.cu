@@ -622,4 +622,79 @@ int clef_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ld
     return CLEF_OK;
 }
 
+// ------------------------------------------------ allocation-free span sums
+
+}  // extern "C"
+
+// Scratch of clef_span_sums_noalloc: the status word (first 256 bytes) and the plan.
+// On the host this name is only a stand-in, not a device address: host code looks
+// the device address up once per device and passes that to the kernel.
+static __device__ __align__(256) uint8_t g_span_sums_scratch[CLEF_SPAN_SUMS_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device (looked up on first use).
+int span_sums_scratch(uint8_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CLEF_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_span_sums_scratch) != cudaSuccess || !p) return CLEF_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = static_cast<uint8_t*>(g_scratch_addr[dev]);
+    return CLEF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int clef_span_sums_noalloc(const clef_config* cfg, const clef_schema* schema, const uint16_t* hidden,
+                           const int32_t* token_ids, const uint16_t* lexical, float* q_sum, float* o_sum,
+                           float* x_sum, void* stream) {
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (!hidden || !token_ids || !lexical || !q_sum || !o_sum || !x_sum) return CLEF_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(hidden) & 15) || (reinterpret_cast<uintptr_t>(lexical) & 15) ||
+        (reinterpret_cast<uintptr_t>(q_sum) & 15) || (reinterpret_cast<uintptr_t>(o_sum) & 15) ||
+        (reinterpret_cast<uintptr_t>(x_sum) & 15))
+        return CLEF_ERR_INVALID_ARGUMENT;
+    const int v = validate_schema(cfg, schema);
+    if (v != CLEF_OK) return v;
+    Plan p;
+    build_plan(cfg, schema, p);
+    constexpr size_t kPlanOff = 256;  // the status word sits in the first 256 bytes
+    if (kPlanOff + p.blob.size() * 4 > CLEF_SPAN_SUMS_NOALLOC_SCRATCH_BYTES) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* scratch = nullptr;
+    const int sa = span_sums_scratch(&scratch);
+    if (sa != CLEF_OK) return sa;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    {
+        const int u = upload_plan(p, scratch, scratch + kPlanOff, st);  // also clears the status word
+        if (u != CLEF_OK) return u;
+    }
+    const int32_t* plan = reinterpret_cast<const int32_t*>(scratch + kPlanOff);
+    SpanPoolArgs sp{};
+    sp.hidden = hidden; sp.row_stride = schema->row_stride; sp.Lpad = schema->Lpad; sp.H = cfg->hidden;
+    sp.vocab = cfg->vocab; sp.token_ids = token_ids; sp.lexical = lexical;
+    sp.item_kind = plan + p.item_kind; sp.item_index = plan + p.item_index;
+    sp.lengths = plan + p.lengths; sp.rec_row_off = plan + p.rec_row_off; sp.rec_q_off = plan + p.rec_q_off;
+    sp.q_rec = plan + p.q_rec; sp.q_span = plan + p.q_span; sp.q_opt_off = plan + p.q_opt_off;
+    sp.o_rec = plan + p.o_rec; sp.o_span = plan + p.o_span;
+    sp.q_sum = q_sum; sp.o_sum = o_sum; sp.x_sum = x_sum;
+    sp.flags = reinterpret_cast<int*>(scratch);
+    CK(launch_span_pool(sp, p.n_items, true, st));
+    int h = 0;
+    CK(cudaMemcpyAsync(&h, scratch, 4, cudaMemcpyDeviceToHost, st));
+    CK(cudaStreamSynchronize(st));
+    if (h & kFlagTimeout) return CLEF_ERR_DEVICE_TIMEOUT;
+    if (h & kFlagBounds) return CLEF_ERR_DEVICE_BOUNDS;
+    return CLEF_OK;
+}
+
 }  // extern "C"
