@@ -39,6 +39,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 __global__ void __launch_bounds__(kThreads, 3)
     route_attn_partial_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                               const RouteAttnArgs a) {
+    griddep_wait();
+    griddep_launch();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
@@ -48,7 +50,11 @@ __global__ void __launch_bounds__(kThreads, 3)
     uint64_t* qbar = empty + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(qbar + 1);
 
-    const int cx = blockIdx.x, h = blockIdx.y, qp = blockIdx.z;
+    // head fastest, then query block: CTAs that run side by side read the K/V rows of
+    // one chunk together (all heads of each row, and every query block's copy via L2)
+    const int h = blockIdx.x % a.heads;
+    const int qp = (blockIdx.x / a.heads) % a.qblocks;
+    const int cx = blockIdx.x / (a.heads * a.qblocks);
     const int b = a.chunk_rec[cx], kc = a.chunk_idx[cx];
     const int o_base = a.rec_o_off[b];
     const int O_b = a.rec_o_off[b + 1] - o_base;
@@ -224,6 +230,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 
 // Merge of the split-L partials of one (option, head): one warp, 2 dims per lane.
 __global__ void __launch_bounds__(256) route_attn_merge_kernel(const RouteAttnArgs a, int O) {
+    griddep_wait();
+    griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int item = blockIdx.x * 8 + warp;
     if (item >= O * a.heads) return;
@@ -262,15 +270,17 @@ cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, int 
         return cudaErrorInvalidValue;
     if (!make_tma_2d_bf16(&tkv, a.kv, uint64_t(a.ldkv), uint64_t(a.kv_rows), uint64_t(a.ldkv), 64))
         return cudaErrorInvalidValue;
-    const int qblocks = (max_rec_options + kQRows - 1) / kQRows;
-    route_attn_partial_kernel<<<dim3(n_chunks, a.heads, qblocks), kThreads, kSmem, s>>>(tq, tkv, a);
-    return counted(cudaGetLastError());
+    RouteAttnArgs aa = a;
+    aa.qblocks = (max_rec_options + kQRows - 1) / kQRows;
+    aa.n_chunks = n_chunks;
+    const int64_t grid = int64_t(aa.qblocks) * n_chunks * a.heads;
+    if (grid >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    return launch_pdl(route_attn_partial_kernel, dim3(unsigned(grid)), dim3(kThreads), kSmem, s, tq, tkv, aa);
 }
 
 cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s) {
     if (O <= 0) return cudaSuccess;
-    route_attn_merge_kernel<<<(O * a.heads + 7) / 8, 256, 0, s>>>(a, O);
-    return counted(cudaGetLastError());
+    return launch_pdl(route_attn_merge_kernel, dim3((O * a.heads + 7) / 8), dim3(256), 0, s, a, O);
 }
 
 }  // namespace clef

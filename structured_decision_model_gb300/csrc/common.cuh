@@ -25,6 +25,14 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+// Programmatic dependent launch: every kernel of the head is launched so that it may
+// start while the previous kernel of the stream drains.  griddep_wait() blocks until
+// the previous grid has completed and its memory is visible, so it comes before the
+// first access to anything an earlier kernel wrote; griddep_launch() lets the next
+// kernel be scheduled early.  Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -163,6 +171,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
+// 32 lanes x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async proxy
+// (tensor-core operand reads through matrix descriptors).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the 128-byte
@@ -175,6 +201,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     d |= uint64_t(1024 >> 4) << 32;      // stride byte offset: next 8-row group
     d |= uint64_t(1) << 46;              // descriptor version
     d |= uint64_t(2) << 61;              // 128-byte swizzle
+    return d;
+}
+
+// Descriptor of an MN-major tile written by TMA with the 128-byte swizzle: each
+// 128-byte row holds 64 consecutive MN elements of one K index, 8-row (8 K) atoms
+// stacked every 1024 bytes along K (stride byte offset).  Covers MN extents of 64.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFFu);
+    d |= uint64_t(1) << 16;              // leading byte offset: next 64-element MN block (unused here)
+    d |= uint64_t(1024 >> 4) << 32;      // stride byte offset: next 8 K rows
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
     return d;
 }
 

@@ -163,6 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_launch();
+    griddep_wait();  // operands and outputs may belong to the previous kernel of the stream
 
     const int n_tiles = args.n_mtiles * args.n_ntiles * args.splits;
     const int kblocks = args.kblocks;
@@ -396,8 +398,7 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     }
     const int tiles = out_tiles * a.splits;
     const int grid = tiles < sms ? tiles : sms;
-    gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, s>>>(ta, tb, a);
-    return counted(cudaGetLastError());
+    return launch_pdl(gemm_tc_kernel<BN>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, a);
 }
 
 }  // namespace

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restri
                                                        const int32_t* __restrict__ rec_row_off,
                                                        const int32_t* __restrict__ lengths, int R,
                                                        float* __restrict__ mu, float* __restrict__ rstd) {
+    griddep_wait();
+    griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + warp;
     if (r >= R) return;
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restri
 // =====================================================================
 template <bool RAW>
 __global__ void __launch_bounds__(256) span_pool_kernel(SpanPoolArgs a) {
+    griddep_wait();
+    griddep_launch();
     const int kind = a.item_kind[blockIdx.x];
     const int idx = a.item_index[blockIdx.x];
     const int H = a.H;
@@ -89,26 +93,45 @@ __global__ void __launch_bounds__(256) span_pool_kernel(SpanPoolArgs a) {
         float acc[8], lex[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) { acc[k] = 0.f; lex[k] = 0.f; }
-        for (int t = s; t < e; ++t) {
-            uint4 w = __ldg(reinterpret_cast<const uint4*>(a.hidden + (rec_base + t) * a.row_stride) + c8);
-            float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                          bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-            if (RAW) {
+        // rows in groups of 4: all loads of a group are issued before its sums, which are
+        // then taken in row order (the same order as one row at a time)
+        for (int t0 = s; t0 < e; t0 += 4) {
+            const int nr = min(4, e - t0);
+            uint4 w[4], x[4];
+            float m[4], rs[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) acc[k] += v[k];
-            } else {
-                const float m = a.mu[stat_base + t], rs = a.rstd[stat_base + t];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) acc[k] += (v[k] - m) * rs;
+            for (int u = 0; u < 4; ++u) {
+                if (u < nr) {
+                    w[u] = __ldg(reinterpret_cast<const uint4*>(a.hidden + (rec_base + t0 + u) * a.row_stride) + c8);
+                    if (!RAW) { m[u] = a.mu[stat_base + t0 + u]; rs[u] = a.rstd[stat_base + t0 + u]; }
+                    x[u] = make_uint4(0, 0, 0, 0);
+                    if (kind == 1) {
+                        const int id = a.token_ids[rec_base + t0 + u];
+                        if (id >= 0 && id < a.vocab)
+                            x[u] = __ldg(reinterpret_cast<const uint4*>(a.lexical + int64_t(id) * H) + c8);
+                        else if (c8 == 0)
+                            atomicOr(a.flags, kFlagBounds);
+                    }
+                }
             }
-            if (kind == 1) {
-                const int id = a.token_ids[rec_base + t];
-                if (id >= 0 && id < a.vocab) {
-                    uint4 x = __ldg(reinterpret_cast<const uint4*>(a.lexical + int64_t(id) * H) + c8);
-                    lex[0] += bf16_lo(x.x); lex[1] += bf16_hi(x.x); lex[2] += bf16_lo(x.y); lex[3] += bf16_hi(x.y);
-                    lex[4] += bf16_lo(x.z); lex[5] += bf16_hi(x.z); lex[6] += bf16_lo(x.w); lex[7] += bf16_hi(x.w);
-                } else if (c8 == 0) {
-                    atomicOr(a.flags, kFlagBounds);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (u < nr) {
+                    const float v[8] = {bf16_lo(w[u].x), bf16_hi(w[u].x), bf16_lo(w[u].y), bf16_hi(w[u].y),
+                                        bf16_lo(w[u].z), bf16_hi(w[u].z), bf16_lo(w[u].w), bf16_hi(w[u].w)};
+                    if (RAW) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) acc[k] += v[k];
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) acc[k] += (v[k] - m[u]) * rs[u];
+                    }
+                    if (kind == 1) {
+                        lex[0] += bf16_lo(x[u].x); lex[1] += bf16_hi(x[u].x);
+                        lex[2] += bf16_lo(x[u].y); lex[3] += bf16_hi(x[u].y);
+                        lex[4] += bf16_lo(x[u].z); lex[5] += bf16_hi(x[u].z);
+                        lex[6] += bf16_lo(x[u].w); lex[7] += bf16_hi(x[u].w);
+                    }
                 }
             }
         }
@@ -181,6 +204,8 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const float* __restrict
                                                         const uint16_t* __restrict__ w,
                                                         const uint16_t* __restrict__ bias,
                                                         uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32) {
+    griddep_wait();
+    griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + warp;
     if (r >= rows) return;
@@ -219,6 +244,8 @@ __global__ void __launch_bounds__(256) field_pool_kernel(const float* __restrict
                                                         const int32_t* __restrict__ q_opt_off,
                                                         const uint16_t* __restrict__ w_a, const uint16_t* __restrict__ b_a,
                                                         uint16_t* __restrict__ out, int64_t ldo, int col_off) {
+    griddep_wait();
+    griddep_launch();
     __shared__ float sc[256];
     const int q = blockIdx.x;
     const int j0 = q_opt_off[q], n = q_opt_off[q + 1] - j0;
@@ -258,6 +285,8 @@ __global__ void __launch_bounds__(256) field_pool_kernel(const float* __restrict
 __global__ void __launch_bounds__(128) field_attn_kernel(const uint16_t* __restrict__ qkv, int D,
                                                         const int32_t* __restrict__ rec_q_off, float scale,
                                                         uint16_t* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     __shared__ float sq[kMaxFields][65], sk[kMaxFields][65], sv[kMaxFields][65];
     __shared__ float sp[kMaxFields][kMaxFields + 1];
     const int b = blockIdx.x, h = blockIdx.y;
@@ -303,6 +332,8 @@ __global__ void __launch_bounds__(128) field_attn_kernel(const uint16_t* __restr
 __global__ void __launch_bounds__(256) build_z_kernel(const float* __restrict__ f_hat, const float* __restrict__ o_hat,
                                                      const int32_t* __restrict__ o_q, int O, int D,
                                                      uint16_t* __restrict__ z) {
+    griddep_wait();
+    griddep_launch();
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= int64_t(O) * D) return;
     const int j = int(i / D), c = int(i % D);
@@ -323,6 +354,8 @@ __global__ void __launch_bounds__(256) build_z_kernel(const float* __restrict__ 
 //   p = softmax over the question's options; answers by question type.
 // =====================================================================
 __global__ void __launch_bounds__(256) score_softmax_kernel(ScoreArgs a) {
+    griddep_wait();
+    griddep_launch();
     __shared__ float s_logit[256];
     __shared__ float s_red[8];
     __shared__ float s_anchor_norm;
@@ -335,7 +368,11 @@ __global__ void __launch_bounds__(256) score_softmax_kernel(ScoreArgs a) {
     const float* g = a.g32 + int64_t(b) * H;
     // |u_q + g_b|
     float ss = 0.f;
-    for (int c = threadIdx.x; c < H; c += blockDim.x) { const float v = u[c] + g[c]; ss += v * v; }
+    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
+        const float4 uv = reinterpret_cast<const float4*>(u)[c], gv = reinterpret_cast<const float4*>(g)[c];
+        const float v0 = uv.x + gv.x, v1 = uv.y + gv.y, v2 = uv.z + gv.z, v3 = uv.w + gv.w;
+        ss += v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3;
+    }
     ss = warp_sum(ss);
     if (lane == 0) s_red[warp] = ss;
     __syncthreads();
@@ -350,16 +387,30 @@ __global__ void __launch_bounds__(256) score_softmax_kernel(ScoreArgs a) {
     const float* f = a.f_hat + int64_t(q) * D;
     for (int jj = warp; jj < n; jj += 8) {
         const int j = j0 + jj;
-        const float* x = a.x32 + int64_t(j) * H;
+        const float4* x4 = reinterpret_cast<const float4*>(a.x32 + int64_t(j) * H);
+        const float4* u4 = reinterpret_cast<const float4*>(u);
+        const float4* g4 = reinterpret_cast<const float4*>(g);
         float xa = 0.f, xx = 0.f;
-        for (int c = lane; c < H; c += 32) { const float xv = x[c]; xa += xv * (u[c] + g[c]); xx += xv * xv; }
-        const float* o = a.o_hat + int64_t(j) * D;
-        const uint16_t* hm = a.mlp_hidden + int64_t(j) * D;
+#pragma unroll 4
+        for (int c = lane; c < H / 4; c += 32) {
+            const float4 xv = x4[c], uv = u4[c], gv = g4[c];
+            xa += xv.x * (uv.x + gv.x) + xv.y * (uv.y + gv.y) + xv.z * (uv.z + gv.z) + xv.w * (uv.w + gv.w);
+            xx += xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
+        }
+        const float4* o4 = reinterpret_cast<const float4*>(a.o_hat + int64_t(j) * D);
+        const float4* f4 = reinterpret_cast<const float4*>(f);
+        const uint2* hm = reinterpret_cast<const uint2*>(a.mlp_hidden + int64_t(j) * D);
+        const uint2* w2 = reinterpret_cast<const uint2*>(a.w2);
         float fo = 0.f, ff = 0.f, oo = 0.f, mm = 0.f;
-        for (int c = lane; c < D; c += 32) {
-            const float fv = f[c], ov = o[c];
-            fo += fv * ov; ff += fv * fv; oo += ov * ov;
-            mm += bf16_to_float(hm[c]) * bf16_to_float(a.w2[c]);
+#pragma unroll 2
+        for (int c = lane; c < D / 4; c += 32) {
+            const float4 fv = f4[c], ov = o4[c];
+            fo += fv.x * ov.x + fv.y * ov.y + fv.z * ov.z + fv.w * ov.w;
+            ff += fv.x * fv.x + fv.y * fv.y + fv.z * fv.z + fv.w * fv.w;
+            oo += ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w;
+            const uint2 hv = hm[c], wv = w2[c];
+            mm += bf16_lo(hv.x) * bf16_lo(wv.x) + bf16_hi(hv.x) * bf16_hi(wv.x) + bf16_lo(hv.y) * bf16_lo(wv.y) +
+                  bf16_hi(hv.y) * bf16_hi(wv.y);
         }
         xa = warp_sum(xa); xx = warp_sum(xx); fo = warp_sum(fo); ff = warp_sum(ff); oo = warp_sum(oo); mm = warp_sum(mm);
         if (lane == 0) {
@@ -441,6 +492,8 @@ struct PlanChunk {
 };
 
 __global__ void __launch_bounds__(256) plan_upload_kernel(int32_t* __restrict__ dst, const PlanChunk c) {
+    griddep_wait();
+    griddep_launch();
     for (int i = threadIdx.x; i < c.n; i += blockDim.x) dst[i] = c.data[i];
 }
 
@@ -462,51 +515,44 @@ cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpa
                              const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,
                              cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
-    row_stats_kernel<<<(R + 7) / 8, 256, 0, s>>>(hidden, row_stride, Lpad, H, tile_rec, rec_row_off, lengths, R, mu,
-                                                 rstd);
-    return counted(cudaGetLastError());
+    return launch_pdl(row_stats_kernel, dim3((R + 7) / 8), dim3(256), 0, s, hidden, row_stride, Lpad, H, tile_rec,
+                      rec_row_off, lengths, R, mu, rstd);
 }
 
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s) {
     if (n_items <= 0) return cudaSuccess;
-    if (raw) span_pool_kernel<true><<<n_items, 256, 0, s>>>(a);
-    else span_pool_kernel<false><<<n_items, 256, 0, s>>>(a);
-    return counted(cudaGetLastError());
+    if (raw) return launch_pdl(span_pool_kernel<true>, dim3(n_items), dim3(256), 0, s, a);
+    return launch_pdl(span_pool_kernel<false>, dim3(n_items), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
                               uint16_t* out_bf16, float* out_f32, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    layer_norm_kernel<<<(rows + 7) / 8, 256, 0, s>>>(x, rows, D, w, b, out_bf16, out_f32);
-    return counted(cudaGetLastError());
+    return launch_pdl(layer_norm_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
 }
 
 cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,
                               const uint16_t* b_a, uint16_t* out, int64_t ldo, int col_off, cudaStream_t s) {
     if (Q <= 0) return cudaSuccess;
-    field_pool_kernel<<<Q, 256, 0, s>>>(o_hat, D, q_opt_off, w_a, b_a, out, ldo, col_off);
-    return counted(cudaGetLastError());
+    return launch_pdl(field_pool_kernel, dim3(Q), dim3(256), 0, s, o_hat, D, q_opt_off, w_a, b_a, out, ldo, col_off);
 }
 
 cudaError_t launch_field_attn(const uint16_t* qkv, int D, int heads, const int32_t* rec_q_off, int B, float scale,
                               uint16_t* out, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    field_attn_kernel<<<dim3(B, heads), 128, 0, s>>>(qkv, D, rec_q_off, scale, out);
-    return counted(cudaGetLastError());
+    return launch_pdl(field_attn_kernel, dim3(B, heads), dim3(128), 0, s, qkv, D, rec_q_off, scale, out);
 }
 
 cudaError_t launch_build_z(const float* f_hat, const float* o_hat, const int32_t* o_q, int O, int D, uint16_t* z,
                            cudaStream_t s) {
     const int64_t n = int64_t(O) * D;
     if (n <= 0) return cudaSuccess;
-    build_z_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(f_hat, o_hat, o_q, O, D, z);
-    return counted(cudaGetLastError());
+    return launch_pdl(build_z_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, s, f_hat, o_hat, o_q, O, D, z);
 }
 
 cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s) {
     if (Q <= 0) return cudaSuccess;
-    score_softmax_kernel<<<Q, 256, 0, s>>>(a);
-    return counted(cudaGetLastError());
+    return launch_pdl(score_softmax_kernel, dim3(Q), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaStream_t s) {
@@ -514,8 +560,7 @@ cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaS
     for (size_t off = 0; off < n; off += kPlanChunkInts) {
         c.n = int32_t(n - off < size_t(kPlanChunkInts) ? n - off : size_t(kPlanChunkInts));
         for (int i = 0; i < c.n; ++i) c.data[i] = src[off + i];
-        plan_upload_kernel<<<1, 256, 0, s>>>(dst + off, c);
-        const cudaError_t e = counted(cudaGetLastError());
+        const cudaError_t e = launch_pdl(plan_upload_kernel, dim3(1), dim3(256), 0, s, dst + off, c);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -44,6 +44,7 @@ struct RouteAttnArgs {
     float* pm; float* pl; float* pacc;    // partials
     uint16_t* out; int64_t ldo;           // [O][D] bf16 merged output
     int* flags;                           // device status word
+    int qblocks, n_chunks;                // grid decomposition (set by the launcher)
 };
 
 struct ScoreArgs {

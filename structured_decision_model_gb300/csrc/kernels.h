@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 namespace clef {
 
@@ -16,6 +17,23 @@ extern std::atomic<uint64_t> g_kernel_launches;
 inline cudaError_t counted(cudaError_t e) {
     if (e == cudaSuccess) g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
     return e;
+}
+
+// Launch with programmatic stream serialization (see griddep_wait in common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return counted(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 
 // ------------------------------------------------------------------ the GEMM
