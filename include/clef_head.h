@@ -148,6 +148,12 @@ typedef struct clef_debug_outputs {
      * [2] [3] the first routing layer's split-L attention kernel, [4] [5] span
      * pooling, [6] [7] memory row statistics. */
     void* events[8];
+    /* Optional launch timeline: when `timeline` is not NULL, the call records
+     * timeline[k] (a cudaEvent_t) on `stream` right after its k-th kernel launch,
+     * for k < timeline_len; the number of launches is written to *timeline_count. */
+    void** timeline;
+    int32_t timeline_len;
+    int32_t* timeline_count;
 } clef_debug_outputs;
 
 /* The forward pass.

@@ -181,10 +181,21 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
     p.item_kind = put(p.n_items);
     p.item_index = put(p.n_items);
     {
-        int i = 0;
-        for (int q = 0; q < Q; ++q, ++i) { v[p.item_kind + i] = 0; v[p.item_index + i] = q; }
-        for (int j = 0; j < O; ++j, ++i) { v[p.item_kind + i] = 1; v[p.item_index + i] = j; }
-        for (int b = 0; b < B; ++b, ++i) { v[p.item_kind + i] = 2; v[p.item_index + i] = b; }
+        // pooling work items, most rows first (option items read two rows per span row),
+        // so that the last wave of CTAs holds the short ones
+        std::vector<std::pair<int, int>> cost;  // (rows read, item id)
+        cost.reserve(p.n_items);
+        for (int q = 0; q < Q; ++q) cost.push_back({s->q_span[2 * q + 1] - s->q_span[2 * q], q});
+        for (int j = 0; j < O; ++j) cost.push_back({2 * (s->o_span[2 * j + 1] - s->o_span[2 * j]), Q + j});
+        for (int b = 0; b < B; ++b) cost.push_back({1, Q + O + b});
+        std::stable_sort(cost.begin(), cost.end(),
+                         [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
+        for (int i = 0; i < p.n_items; ++i) {
+            const int id = cost[i].second;
+            const int kind = id < Q ? 0 : (id < Q + O ? 1 : 2);
+            v[p.item_kind + i] = kind;
+            v[p.item_index + i] = kind == 0 ? id : (kind == 1 ? id - Q : id - Q - O);
+        }
     }
     p.n_chunks = nch;
     p.chunk_rec = put(nch);
@@ -390,6 +401,13 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
     if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int n_launch = 0;
+    // records the next timeline event (if asked for) after a launch
+    auto tick = [&]() -> cudaError_t {
+        const int k = n_launch++;
+        if (!debug || !debug->timeline || k >= debug->timeline_len || !debug->timeline[k]) return cudaSuccess;
+        return cudaEventRecord(static_cast<cudaEvent_t>(debug->timeline[k]), st);
+    };
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const uint8_t* pw = static_cast<const uint8_t*>(prepared);
     const PreparedLayout PL(cfg);
@@ -431,7 +449,7 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
     // 1. memory row statistics (the memory LayerNorm is applied through them)
     CK(mark(debug, 6, st));
     CK(launch_row_stats(hidden, schema->row_stride, schema->Lpad, H, T(p.tile_rec), T(p.rec_row_off), T(p.lengths),
-                        p.R, mu, rstd, st));
+                        p.R, mu, rstd, st)); CK(tick());
     CK(mark(debug, 7, st));
     // 2. span pooling
     SpanPoolArgs sp{};
@@ -447,13 +465,13 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
     sp.dbg_c = debug ? debug->pooled_c : nullptr;
     sp.flags = flags;
     CK(mark(debug, 4, st));
-    CK(launch_span_pool(sp, p.n_items, false, st));
+    CK(launch_span_pool(sp, p.n_items, false, st)); CK(tick());
     CK(mark(debug, 5, st));
     // 3. option queries: o = [c | x | u] [W_ctx | W_lex | W_qst]^T + b
     {
         GemmEpilogue e;
         e.kind = EPI_F32; e.bias_bf16 = W(weights, 5); e.out = o_res; e.ldo = D;
-        CK(dense(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, e, flags, st, sk));
+        CK(dense(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, e, flags, st, sk)); CK(tick());
     }
     // 4. memory K/V of every routing layer (LayerNorm folded), real rows only
     {
@@ -467,7 +485,7 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
         e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
         e.out = kv; e.ldo = NKV; e.M = p.R;
         CK(mark(debug, 0, st));
-        CK(launch_gemm(g, e, flags, st));
+        CK(launch_gemm(g, e, flags, st)); CK(tick());
         CK(mark(debug, 1, st));
     }
     // 5. evidence routing layers
@@ -480,63 +498,63 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
     ra.pm = reinterpret_cast<float*>(ws + L.pm); ra.pl = reinterpret_cast<float*>(ws + L.pl);
     ra.pacc = reinterpret_cast<float*>(ws + L.pacc); ra.out = attn_buf; ra.ldo = D;
     for (int l = 0; l < cfg->n_route; ++l) {
-        CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 0)), W(weights, wi.route(l, 1)), ln_buf, nullptr, st));
+        CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 0)), W(weights, wi.route(l, 1)), ln_buf, nullptr, st)); CK(tick());
         GemmEpilogue eq;
         eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.route(l, 3)); eq.out = q_buf; eq.ldo = D;
-        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 2)), D, D, eq, flags, st, sk));
+        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 2)), D, D, eq, flags, st, sk)); CK(tick());
         ra.k_col = 2 * l * D;
         ra.v_col = (2 * l + 1) * D;
         if (l == 0) CK(mark(debug, 2, st));
-        CK(launch_route_attn_partial(ra, p.n_chunks, O, p.max_rec_options, st));
+        CK(launch_route_attn_partial(ra, p.n_chunks, O, p.max_rec_options, st)); CK(tick());
         if (l == 0) CK(mark(debug, 3, st));
-        CK(launch_route_attn_merge(ra, O, st));
+        CK(launch_route_attn_merge(ra, O, st)); CK(tick());
         GemmEpilogue eo;
         eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.route(l, 9)); eo.out = o_res; eo.ldo = D;
-        CK(dense(attn_buf, D, O, W(weights, wi.route(l, 8)), D, D, eo, flags, st, sk));
+        CK(dense(attn_buf, D, O, W(weights, wi.route(l, 8)), D, D, eo, flags, st, sk)); CK(tick());
         CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 10)), W(weights, wi.route(l, 11)), ln_buf, nullptr,
-                             st));
+                             st)); CK(tick());
         GemmEpilogue e1;
         e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.route(l, 13)); e1.out = hid_buf; e1.ldo = F;
-        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 12)), F, D, e1, flags, st, sk));
+        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 12)), F, D, e1, flags, st, sk)); CK(tick());
         GemmEpilogue e2;
         e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.route(l, 15)); e2.out = o_res; e2.ldo = D;
-        CK(dense(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, e2, flags, st, sk));
+        CK(dense(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, e2, flags, st, sk)); CK(tick());
     }
-    CK(launch_layer_norm(o_res, O, D, W(weights, wi.mid(0)), W(weights, wi.mid(1)), nullptr, o_hat, st));
+    CK(launch_layer_norm(o_res, O, D, W(weights, wi.mid(0)), W(weights, wi.mid(1)), nullptr, o_hat, st)); CK(tick());
     // 6. fields: [u | g | summary] [W_fu | W_fg | W_fs]^T + b + type embedding
     CK(launch_field_pool(o_hat, D, T(p.q_opt_off), Q, W(weights, wi.mid(2)), W(weights, wi.mid(3)), a_field, ld_field,
-                         2 * H, st));
+                         2 * H, st)); CK(tick());
     {
         GemmEpilogue e;
         e.kind = EPI_F32; e.bias_bf16 = W(weights, wi.mid(7)); e.row_table = W(weights, wi.mid(8));
         e.row_idx = T(p.q_type); e.ld_table = D; e.out = f_res; e.ldo = D;
-        CK(dense(a_field, ld_field, Q, reinterpret_cast<const uint16_t*>(pw + PL.wfield), D, ld_field, e, flags, st, sk));
+        CK(dense(a_field, ld_field, Q, reinterpret_cast<const uint16_t*>(pw + PL.wfield), D, ld_field, e, flags, st, sk)); CK(tick());
     }
     // 7. joint layers over each record's fields
     for (int i = 0; i < cfg->n_joint; ++i) {
-        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 0)), W(weights, wi.joint(i, 1)), ln_buf, nullptr, st));
+        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 0)), W(weights, wi.joint(i, 1)), ln_buf, nullptr, st)); CK(tick());
         GemmEpilogue eq;
         eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.joint(i, 3)); eq.out = q_buf; eq.ldo = 3 * D;
-        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 2)), 3 * D, D, eq, flags, st, sk));
-        CK(launch_field_attn(q_buf, D, cfg->heads, T(p.rec_q_off), B, 0.125f, attn_buf, st));
+        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 2)), 3 * D, D, eq, flags, st, sk)); CK(tick());
+        CK(launch_field_attn(q_buf, D, cfg->heads, T(p.rec_q_off), B, 0.125f, attn_buf, st)); CK(tick());
         GemmEpilogue eo;
         eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.joint(i, 5)); eo.out = f_res; eo.ldo = D;
-        CK(dense(attn_buf, D, Q, W(weights, wi.joint(i, 4)), D, D, eo, flags, st, sk));
-        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 6)), W(weights, wi.joint(i, 7)), ln_buf, nullptr, st));
+        CK(dense(attn_buf, D, Q, W(weights, wi.joint(i, 4)), D, D, eo, flags, st, sk)); CK(tick());
+        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 6)), W(weights, wi.joint(i, 7)), ln_buf, nullptr, st)); CK(tick());
         GemmEpilogue e1;
         e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.joint(i, 9)); e1.out = hid_buf; e1.ldo = F;
-        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 8)), F, D, e1, flags, st, sk));
+        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 8)), F, D, e1, flags, st, sk)); CK(tick());
         GemmEpilogue e2;
         e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.joint(i, 11)); e2.out = f_res; e2.ldo = D;
-        CK(dense(hid_buf, F, Q, W(weights, wi.joint(i, 10)), D, F, e2, flags, st, sk));
+        CK(dense(hid_buf, F, Q, W(weights, wi.joint(i, 10)), D, F, e2, flags, st, sk)); CK(tick());
     }
-    CK(launch_layer_norm(f_res, Q, D, W(weights, wi.tail(0)), W(weights, wi.tail(1)), nullptr, f_hat, st));
+    CK(launch_layer_norm(f_res, Q, D, W(weights, wi.tail(0)), W(weights, wi.tail(1)), nullptr, f_hat, st)); CK(tick());
     // 8. scorer MLP hidden layer, then scores, softmax and answers
-    CK(launch_build_z(f_hat, o_hat, T(p.o_q), O, D, z, st));
+    CK(launch_build_z(f_hat, o_hat, T(p.o_q), O, D, z, st)); CK(tick());
     {
         GemmEpilogue e;
         e.kind = EPI_BF16; e.gelu = 1; e.bias_bf16 = W(weights, wi.tail(5)); e.out = hid_buf; e.ldo = D;
-        CK(dense(z, 4 * D, O, W(weights, wi.tail(4)), D, 4 * D, e, flags, st, sk));
+        CK(dense(z, 4 * D, O, W(weights, wi.tail(4)), D, 4 * D, e, flags, st, sk)); CK(tick());
     }
     ScoreArgs sc{};
     sc.H = H; sc.D = D; sc.q_rec = T(p.q_rec); sc.q_type = T(p.q_type); sc.q_opt_off = T(p.q_opt_off);
@@ -544,7 +562,8 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
     sc.w2 = W(weights, wi.tail(6)); sc.b2 = W(weights, wi.tail(7)); sc.gate = W(weights, wi.tail(2));
     sc.joint_scale = W(weights, wi.tail(3));
     sc.logits = logits; sc.probs = probs; sc.q_value = q_value; sc.q_conf = q_conf; sc.q_argmax = q_argmax;
-    CK(launch_score_softmax(sc, Q, st));
+    CK(launch_score_softmax(sc, Q, st)); CK(tick());
+    if (debug && debug->timeline_count) CK(cudaMemcpyAsync(debug->timeline_count, &n_launch, 4, cudaMemcpyHostToDevice, st));
     if (debug) {
         if (debug->pooled_u) CK(cudaMemcpyAsync(debug->pooled_u, u32, size_t(Q) * H * 4, cudaMemcpyDeviceToDevice, st));
         if (debug->pooled_x) CK(cudaMemcpyAsync(debug->pooled_x, x32, size_t(O) * H * 4, cudaMemcpyDeviceToDevice, st));
