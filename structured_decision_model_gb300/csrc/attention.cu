@@ -149,31 +149,36 @@ __global__ void __launch_bounds__(kThreads, 3)
                 }
             }
             const int kbase = t0 + kt * kKT;
+            if (kbase + kKT > t1) {  // only the chunk's last tile can hold keys past its end
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (kbase + j * 8 + tq * 2 + (c & 1) >= t1) s[j][c] = -INFINITY;
+            }
+            // raw-score row maxima; the scale is applied once per row and fused into the
+            // exponent below (p = 2^(s * scale - m))
             float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int key = kbase + j * 8 + tq * 2 + (c & 1);
-                    const float v = key < t1 ? s[j][c] * sl2 : -INFINITY;
-                    s[j][c] = v;
-                    mx[c >> 1] = fmaxf(mx[c >> 1], v);
-                }
+                mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
+                mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
             }
-            float corr[2], ps[2] = {0.f, 0.f};
+            float corr[2], ps[2] = {0.f, 0.f}, nm[2];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float mn = fmaxf(m_r[r], mx[r]);
-                corr[r] = exp2f(m_r[r] - mn);
+                const float mn = fmaxf(m_r[r], mx[r] * sl2);
+                corr[r] = ex2_approx(m_r[r] - mn);
                 m_r[r] = mn;
+                nm[r] = -mn;
             }
             uint32_t pa[4][4];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float p0 = exp2f(s[j][0] - m_r[0]), p1 = exp2f(s[j][1] - m_r[0]);
-                const float p2 = exp2f(s[j][2] - m_r[1]), p3 = exp2f(s[j][3] - m_r[1]);
+                const float p0 = ex2_approx(fmaf(s[j][0], sl2, nm[0])), p1 = ex2_approx(fmaf(s[j][1], sl2, nm[0]));
+                const float p2 = ex2_approx(fmaf(s[j][2], sl2, nm[1])), p3 = ex2_approx(fmaf(s[j][3], sl2, nm[1]));
                 ps[0] += p0 + p1;
                 ps[1] += p2 + p3;
                 pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);

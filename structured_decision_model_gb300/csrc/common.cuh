@@ -48,6 +48,13 @@ __device__ __forceinline__ uint16_t float_to_bf16(float f) {
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// 2^x with the hardware approximation instruction (about 2 ulp; -inf gives 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float gelu_exact(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
