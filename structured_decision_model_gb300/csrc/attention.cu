@@ -164,16 +164,34 @@ __global__ void __launch_bounds__(kThreads, 3)
                 mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
                 mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
             }
-            float corr[2], ps[2] = {0.f, 0.f}, nm[2];
+            // The row's reference maximum m moves only when a tile's maximum exceeds it by
+            // more than 2^8 (p never exceeds 2^8, so nothing overflows); the accumulator and
+            // the running sum are rescaled only then, which after the first tile is rare.
+            float ps[2] = {0.f, 0.f}, nm[2];
+            bool need[2];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float mn = fmaxf(m_r[r], mx[r] * sl2);
-                corr[r] = ex2_approx(m_r[r] - mn);
-                m_r[r] = mn;
-                nm[r] = -mn;
+                mx[r] *= sl2;
+                need[r] = mx[r] > m_r[r] + 8.f;
             }
+            if (__any_sync(0xffffffffu, need[0] || need[1])) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float mn = need[r] ? mx[r] : m_r[r];
+                    const float corr = ex2_approx(m_r[r] - mn);
+                    m_r[r] = mn;
+                    l_r[r] *= corr;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        acc[j][2 * r] *= corr;
+                        acc[j][2 * r + 1] *= corr;
+                    }
+                }
+            }
+            nm[0] = -m_r[0];
+            nm[1] = -m_r[1];
             uint32_t pa[4][4];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -185,12 +203,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
             }
 #pragma unroll
-            for (int r = 0; r < 2; ++r) l_r[r] = l_r[r] * corr[r] + ps[r];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                acc[j][0] *= corr[0]; acc[j][1] *= corr[0];
-                acc[j][2] *= corr[1]; acc[j][3] *= corr[1];
-            }
+            for (int r = 0; r < 2; ++r) l_r[r] += ps[r];
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll

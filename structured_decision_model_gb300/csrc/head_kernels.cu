@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restri
 // rows instead (the bit-exact index check).
 // =====================================================================
 template <bool RAW>
-__global__ void __launch_bounds__(256) span_pool_kernel(SpanPoolArgs a) {
+__global__ void __launch_bounds__(256, 4) span_pool_kernel(SpanPoolArgs a) {
     griddep_wait();
     griddep_launch();
     const int kind = a.item_kind[blockIdx.x];
@@ -94,24 +94,17 @@ __global__ void __launch_bounds__(256) span_pool_kernel(SpanPoolArgs a) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) { acc[k] = 0.f; lex[k] = 0.f; }
         // rows in groups of 4: all loads of a group are issued before its sums, which are
-        // then taken in row order (the same order as one row at a time)
+        // then taken in row order (the same order as one row at a time); the hidden rows and
+        // the lexical rows of an option span are two separate passes (fewer live registers)
         for (int t0 = s; t0 < e; t0 += 4) {
             const int nr = min(4, e - t0);
-            uint4 w[4], x[4];
+            uint4 w[4];
             float m[4], rs[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 if (u < nr) {
                     w[u] = __ldg(reinterpret_cast<const uint4*>(a.hidden + (rec_base + t0 + u) * a.row_stride) + c8);
                     if (!RAW) { m[u] = a.mu[stat_base + t0 + u]; rs[u] = a.rstd[stat_base + t0 + u]; }
-                    x[u] = make_uint4(0, 0, 0, 0);
-                    if (kind == 1) {
-                        const int id = a.token_ids[rec_base + t0 + u];
-                        if (id >= 0 && id < a.vocab)
-                            x[u] = __ldg(reinterpret_cast<const uint4*>(a.lexical + int64_t(id) * H) + c8);
-                        else if (c8 == 0)
-                            atomicOr(a.flags, kFlagBounds);
-                    }
                 }
             }
 #pragma unroll
@@ -126,12 +119,30 @@ __global__ void __launch_bounds__(256) span_pool_kernel(SpanPoolArgs a) {
 #pragma unroll
                         for (int k = 0; k < 8; ++k) acc[k] += (v[k] - m[u]) * rs[u];
                     }
-                    if (kind == 1) {
-                        lex[0] += bf16_lo(x[u].x); lex[1] += bf16_hi(x[u].x);
-                        lex[2] += bf16_lo(x[u].y); lex[3] += bf16_hi(x[u].y);
-                        lex[4] += bf16_lo(x[u].z); lex[5] += bf16_hi(x[u].z);
-                        lex[6] += bf16_lo(x[u].w); lex[7] += bf16_hi(x[u].w);
+                }
+            }
+        }
+        if (kind == 1) {
+            for (int t0 = s; t0 < e; t0 += 4) {
+                const int nr = min(4, e - t0);
+                uint4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    x[u] = make_uint4(0, 0, 0, 0);
+                    if (u < nr) {
+                        const int id = a.token_ids[rec_base + t0 + u];
+                        if (id >= 0 && id < a.vocab)
+                            x[u] = __ldg(reinterpret_cast<const uint4*>(a.lexical + int64_t(id) * H) + c8);
+                        else if (c8 == 0)
+                            atomicOr(a.flags, kFlagBounds);
                     }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    lex[0] += bf16_lo(x[u].x); lex[1] += bf16_hi(x[u].x);
+                    lex[2] += bf16_lo(x[u].y); lex[3] += bf16_hi(x[u].y);
+                    lex[4] += bf16_lo(x[u].z); lex[5] += bf16_hi(x[u].z);
+                    lex[6] += bf16_lo(x[u].w); lex[7] += bf16_hi(x[u].w);
                 }
             }
         }
