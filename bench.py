@@ -184,6 +184,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--records", type=int, default=0, help="use only the first N records (profiling cases)")
+    ap.add_argument("--stream-chunk", type=int, default=64,
+                    help="rows per chunk of the streaming-ingestion leg (0: skip the leg)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -334,6 +336,38 @@ def main():
             e2e_ms = float(t.item())
         e2e_value = world * bt.B / (e2e_ms / 1e3)
 
+    # streaming ingestion: memory rows arrive in chunks (records interleaved); the head
+    # finishes after the last chunk.  finish_ms is the latency from the last chunk to the
+    # answers, to compare with a whole forward's ms_per_step.
+    stream_info = None
+    if args.stream_chunk > 0:
+        C = args.stream_chunk
+        chunks = [(b, r0, min(C, int(bt.lengths[b]) - r0)) for r0 in range(0, int(bt.lengths.max()), C)
+                  for b in range(bt.B) if r0 < bt.lengths[b]]
+
+        def stream_pass(ev=None):
+            head.stream_begin(schema)
+            for (b, r0, n) in chunks:
+                head.stream_rows(schema, hidden, b, r0, n)
+            if ev is not None:
+                ev.record(stream)
+            head.stream_finish(schema, hidden, ids, lexical, out=out)
+
+        stream_pass()
+        torch.cuda.synchronize()
+        s0, s1, s2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        t_host = time.perf_counter()
+        s0.record(stream)
+        stream_pass(s1)
+        s2.record(stream)
+        torch.cuda.synchronize()
+        t_host = time.perf_counter() - t_host
+        if head.device_status() != 0:
+            raise RuntimeError("device status after the streaming leg is not OK")
+        stream_info = {"chunk_rows": C, "chunks": len(chunks), "finish_ms": s1.elapsed_time(s2),
+                       "ingest_ms": s0.elapsed_time(s1), "host_us_per_chunk": t_host * 1e6 / len(chunks),
+                       "forward_ms": ms}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         b0 = 0
@@ -376,6 +410,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": "records/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "timing": "host wall clock around e2e steps, input copies double-buffered on a copy stream"},
             "gpu_launches": int(launches),
+            "stream": stream_info,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))

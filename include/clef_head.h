@@ -181,6 +181,38 @@ CLEF_API int clef_head_forward(const clef_config* cfg, const void* const* weight
                       float* q_conf, int32_t* q_argmax, void* workspace, size_t workspace_bytes,
                       const clef_debug_outputs* debug, void* stream);
 
+/* Streaming memory ingestion.  A backbone may produce the final-norm hidden rows of a
+ * record in chunks ("clef-flash-CoreAI metadata.json" decision.readout: a row of T ids
+ * runs as ceil(T / 64) calls of 64 positions, whose hidden rows are concatenated).  The
+ * schema (and so every record's final length and spans) is known before the first
+ * chunk, because the encoder lays the whole prompt out first.  The memory part of the
+ * head (row statistics and the K/V projection, its dominant cost) can then run chunk
+ * by chunk while the backbone produces later rows:
+ *   clef_stream_begin   once per batch: validates the schema, uploads its launch plan
+ *                       into `workspace` and clears the status word;
+ *   clef_stream_rows    whenever rows [row0, row0 + n_rows) of record `record` are
+ *                       final in `hidden` (same layout as for clef_head_forward):
+ *                       computes their statistics and K/V into the workspace.  Chunks
+ *                       of any size, in any order; every real row exactly once.
+ *                       0 <= row0, 1 <= n_rows, row0 + n_rows <= lengths[record].
+ *   clef_stream_finish  after every real row of every record went through
+ *                       clef_stream_rows: the rest of the head (pooling, routing,
+ *                       fields, joint layers, scorer, softmax), with the same arguments
+ *                       and outputs as clef_head_forward.
+ * The outputs equal clef_head_forward's on the same inputs.  All calls of one batch use
+ * the same schema, prepared weights and workspace (sized by clef_workspace_size), on
+ * one stream; the workspace must not be used by other calls in between. */
+CLEF_API int clef_stream_begin(const clef_config* cfg, const clef_schema* schema, void* workspace,
+                               size_t workspace_bytes, void* stream);
+CLEF_API int clef_stream_rows(const clef_config* cfg, const void* prepared, const clef_schema* schema,
+                              const uint16_t* hidden, int32_t record, int32_t row0, int32_t n_rows,
+                              void* workspace, size_t workspace_bytes, void* stream);
+CLEF_API int clef_stream_finish(const clef_config* cfg, const void* const* weights, const void* prepared,
+                                const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
+                                const uint16_t* lexical, float* logits, float* probs, float* q_value,
+                                float* q_conf, int32_t* q_argmax, void* workspace, size_t workspace_bytes,
+                                const clef_debug_outputs* debug, void* stream);
+
 /* Waits for `stream`, then reads and clears the device-side status word kept at the
  * start of `workspace`: CLEF_OK, CLEF_ERR_DEVICE_BOUNDS or CLEF_ERR_DEVICE_TIMEOUT.
  * Every clef_head_forward / clef_span_sums call clears that word when it starts, so

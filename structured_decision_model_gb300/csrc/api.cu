@@ -378,11 +378,20 @@ int clef_workspace_size(const clef_config* cfg, const clef_schema* schema, size_
     return CLEF_OK;
 }
 
-int clef_head_forward(const clef_config* cfg, const void* const* weights, const void* prepared,
-                      const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
-                      const uint16_t* lexical, float* logits, float* probs, float* q_value, float* q_conf,
-                      int32_t* q_argmax, void* workspace, size_t workspace_bytes, const clef_debug_outputs* debug,
-                      void* stream) {
+}  // extern "C"
+
+namespace {
+
+enum ForwardMode { kForwardFull = 0, kForwardAfterStream = 1 };
+
+// The forward pass.  kForwardFull uploads the plan and computes the memory statistics
+// and K/V itself; kForwardAfterStream finds both already in the workspace (put there by
+// clef_stream_begin / clef_stream_rows) and only zeroes the records' round-up slack rows.
+int forward_impl(const clef_config* cfg, const void* const* weights, const void* prepared,
+                 const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
+                 const uint16_t* lexical, float* logits, float* probs, float* q_value, float* q_conf,
+                 int32_t* q_argmax, void* workspace, size_t workspace_bytes, const clef_debug_outputs* debug,
+                 void* stream, int mode) {
     if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
     if (!weights || !prepared || !hidden || !token_ids || !lexical || !logits || !probs || !q_value || !q_conf ||
         !q_argmax || !workspace)
@@ -419,7 +428,7 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
     const int H = cfg->hidden, D = cfg->width, F = cfg->ffn, NKV = 2 * cfg->n_route * D;
     const int B = p.B, Q = p.Q, O = p.O;
 
-    {
+    if (mode == kForwardFull) {
         const int u = upload_plan(p, ws, ws + L.plan, st);
         if (u != CLEF_OK) return u;
     }
@@ -447,10 +456,12 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
     const int ld_field = 2 * H + D;
 
     // 1. memory row statistics (the memory LayerNorm is applied through them)
-    CK(mark(debug, 6, st));
-    CK(launch_row_stats(hidden, schema->row_stride, schema->Lpad, H, T(p.tile_rec), T(p.rec_row_off), T(p.lengths),
-                        p.R, mu, rstd, st)); CK(tick());
-    CK(mark(debug, 7, st));
+    if (mode == kForwardFull) {
+        CK(mark(debug, 6, st));
+        CK(launch_row_stats(hidden, schema->row_stride, schema->Lpad, H, T(p.tile_rec), T(p.rec_row_off),
+                            T(p.lengths), p.R, mu, rstd, st)); CK(tick());
+        CK(mark(debug, 7, st));
+    }
     // 2. span pooling
     SpanPoolArgs sp{};
     sp.hidden = hidden; sp.row_stride = schema->row_stride; sp.Lpad = schema->Lpad; sp.H = H; sp.vocab = cfg->vocab;
@@ -474,7 +485,11 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
         CK(dense(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, e, flags, st, sk)); CK(tick());
     }
     // 4. memory K/V of every routing layer (LayerNorm folded), real rows only
-    {
+    if (mode == kForwardAfterStream) {
+        // K/V rows came in chunk by chunk; the round-up slack rows of each record were never
+        // written, and attention reads whole tiles, so they are zeroed here
+        CK(launch_zero_slack(kv, NKV, T(p.rec_row_off), T(p.lengths), B, st)); CK(tick());
+    } else {
         GemmProblem g;
         g.A = hidden; g.lda = schema->row_stride; g.a_rows = int64_t(B) * schema->Lpad;
         g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
@@ -574,6 +589,81 @@ int clef_head_forward(const clef_config* cfg, const void* const* weights, const 
             CK(cudaMemcpyAsync(debug->field_final, f_hat, size_t(Q) * D * 4, cudaMemcpyDeviceToDevice, st));
     }
     return CLEF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int clef_head_forward(const clef_config* cfg, const void* const* weights, const void* prepared,
+                      const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
+                      const uint16_t* lexical, float* logits, float* probs, float* q_value, float* q_conf,
+                      int32_t* q_argmax, void* workspace, size_t workspace_bytes, const clef_debug_outputs* debug,
+                      void* stream) {
+    return forward_impl(cfg, weights, prepared, schema, hidden, token_ids, lexical, logits, probs, q_value, q_conf,
+                        q_argmax, workspace, workspace_bytes, debug, stream, kForwardFull);
+}
+
+int clef_stream_begin(const clef_config* cfg, const clef_schema* schema, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return CLEF_ERR_INVALID_ARGUMENT;
+    const int v = validate_schema(cfg, schema);
+    if (v != CLEF_OK) return v;
+    Plan p;
+    build_plan(cfg, schema, p);
+    const WsLayout L(cfg, p);
+    if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return upload_plan(p, ws, ws + L.plan, static_cast<cudaStream_t>(stream));
+}
+
+int clef_stream_rows(const clef_config* cfg, const void* prepared, const clef_schema* schema, const uint16_t* hidden,
+                     int32_t record, int32_t row0, int32_t n_rows, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (!prepared || !hidden || !workspace || (reinterpret_cast<uintptr_t>(hidden) & 15) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(prepared) & 255))
+        return CLEF_ERR_INVALID_ARGUMENT;
+    const int v = validate_schema(cfg, schema);
+    if (v != CLEF_OK) return v;
+    if (record < 0 || record >= schema->B || row0 < 0 || n_rows < 1 ||
+        int64_t(row0) + n_rows > schema->lengths[record])
+        return CLEF_ERR_INVALID_ARGUMENT;
+    Plan p;
+    build_plan(cfg, schema, p);
+    const WsLayout L(cfg, p);
+    if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* pw = static_cast<const uint8_t*>(prepared);
+    const PreparedLayout PL(cfg);
+    const int H = cfg->hidden, NKV = 2 * cfg->n_route * cfg->width;
+    const int64_t out_row = p.blob[p.rec_row_off + record] + int64_t(row0);  // compact row of the first row
+    const uint16_t* rows = hidden + (int64_t(record) * schema->Lpad + row0) * schema->row_stride;
+    float* mu = reinterpret_cast<float*>(ws + L.mu) + out_row;
+    float* rstd = reinterpret_cast<float*>(ws + L.rstd) + out_row;
+    CK(launch_row_stats_rows(rows, schema->row_stride, H, n_rows, mu, rstd, st));
+    GemmProblem g;
+    g.A = rows; g.lda = schema->row_stride; g.a_rows = n_rows;
+    g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
+    g.N = NKV; g.K = H; g.n_mtiles = (n_rows + kTile - 1) / kTile;
+    GemmEpilogue e;
+    e.kind = EPI_KV_LNFOLD; e.row_mu = mu; e.row_rstd = rstd;
+    e.col_c = reinterpret_cast<const float*>(pw + PL.ckv);
+    e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
+    e.out = reinterpret_cast<uint16_t*>(ws + L.kv) + out_row * NKV; e.ldo = NKV; e.M = n_rows;
+    CK(launch_gemm(g, e, reinterpret_cast<int*>(ws + L.flags), st));
+    return CLEF_OK;
+}
+
+int clef_stream_finish(const clef_config* cfg, const void* const* weights, const void* prepared,
+                       const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
+                       const uint16_t* lexical, float* logits, float* probs, float* q_value, float* q_conf,
+                       int32_t* q_argmax, void* workspace, size_t workspace_bytes, const clef_debug_outputs* debug,
+                       void* stream) {
+    return forward_impl(cfg, weights, prepared, schema, hidden, token_ids, lexical, logits, probs, q_value, q_conf,
+                        q_argmax, workspace, workspace_bytes, debug, stream, kForwardAfterStream);
 }
 
 int clef_device_status(void* workspace, void* stream) {

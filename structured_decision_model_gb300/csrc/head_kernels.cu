@@ -15,23 +15,11 @@ namespace clef {
 // applied through these statistics by the K/V projection epilogue and by pooling.
 // Rows in a record's round-up slack get mu = rstd = 0.
 // =====================================================================
-__global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restrict__ hidden, int64_t row_stride,
-                                                       int Lpad, int H, const int32_t* __restrict__ tile_rec,
-                                                       const int32_t* __restrict__ rec_row_off,
-                                                       const int32_t* __restrict__ lengths, int R,
-                                                       float* __restrict__ mu, float* __restrict__ rstd) {
-    griddep_wait();
-    griddep_launch();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 8 + warp;
-    if (r >= R) return;
-    const int b = tile_rec[r >> 7];
-    const int t = r - rec_row_off[b];
-    if (t >= lengths[b]) {
-        if (lane == 0) { mu[r] = 0.f; rstd[r] = 0.f; }
-        return;
-    }
-    const uint4* row = reinterpret_cast<const uint4*>(hidden + (int64_t(b) * Lpad + t) * row_stride);
+// Mean and 1/sqrt(var + eps) of one bf16 row (one warp; two passes over the row, the
+// second served from L1).
+__device__ __forceinline__ void row_moments(const uint16_t* __restrict__ rowp, int H, int lane, float& mean,
+                                            float& rstd_out) {
+    const uint4* row = reinterpret_cast<const uint4*>(rowp);
     const int n8 = H >> 3;
     float s = 0.f;
 #pragma unroll 4
@@ -51,11 +39,63 @@ __global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restri
         d = bf16_lo(w.z) - m; q += d * d; d = bf16_hi(w.z) - m; q += d * d;
         d = bf16_lo(w.w) - m; q += d * d; d = bf16_hi(w.w) - m; q += d * d;
     }
-    const float var = warp_sum(q) / float(H);
+    mean = m;
+    rstd_out = rsqrtf(warp_sum(q) / float(H) + 1e-5f);
+}
+
+__global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restrict__ hidden, int64_t row_stride,
+                                                       int Lpad, int H, const int32_t* __restrict__ tile_rec,
+                                                       const int32_t* __restrict__ rec_row_off,
+                                                       const int32_t* __restrict__ lengths, int R,
+                                                       float* __restrict__ mu, float* __restrict__ rstd) {
+    griddep_wait();
+    griddep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= R) return;
+    const int b = tile_rec[r >> 7];
+    const int t = r - rec_row_off[b];
+    if (t >= lengths[b]) {
+        if (lane == 0) { mu[r] = 0.f; rstd[r] = 0.f; }
+        return;
+    }
+    float m, rs;
+    row_moments(hidden + (int64_t(b) * Lpad + t) * row_stride, H, lane, m, rs);
     if (lane == 0) {
         mu[r] = m;
-        rstd[r] = rsqrtf(var + 1e-5f);
+        rstd[r] = rs;
     }
+}
+
+// Statistics of n consecutive real rows (streamed memory rows of one record).
+__global__ void __launch_bounds__(256) row_stats_rows_kernel(const uint16_t* __restrict__ rows, int64_t row_stride,
+                                                            int H, int n, float* __restrict__ mu,
+                                                            float* __restrict__ rstd) {
+    griddep_wait();
+    griddep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= n) return;
+    float m, rs;
+    row_moments(rows + int64_t(r) * row_stride, H, lane, m, rs);
+    if (lane == 0) {
+        mu[r] = m;
+        rstd[r] = rs;
+    }
+}
+
+// Zeroes K/V rows L_b .. roundup(L_b, 128) - 1 of every record (one CTA per record).
+__global__ void __launch_bounds__(256) zero_slack_kernel(uint16_t* __restrict__ kv, int ldkv,
+                                                        const int32_t* __restrict__ rec_row_off,
+                                                        const int32_t* __restrict__ lengths) {
+    griddep_wait();
+    griddep_launch();
+    const int b = blockIdx.x;
+    const int L = lengths[b];
+    const int slack = (L + 127) / 128 * 128 - L;
+    uint4* base = reinterpret_cast<uint4*>(kv + (int64_t(rec_row_off[b]) + L) * ldkv);
+    const int n = slack * (ldkv / 8);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
 }
 
 // =====================================================================
@@ -528,6 +568,18 @@ cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpa
     if (R <= 0) return cudaSuccess;
     return launch_pdl(row_stats_kernel, dim3((R + 7) / 8), dim3(256), 0, s, hidden, row_stride, Lpad, H, tile_rec,
                       rec_row_off, lengths, R, mu, rstd);
+}
+
+cudaError_t launch_row_stats_rows(const uint16_t* rows, int64_t row_stride, int H, int n, float* mu, float* rstd,
+                                  cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    return launch_pdl(row_stats_rows_kernel, dim3((n + 7) / 8), dim3(256), 0, s, rows, row_stride, H, n, mu, rstd);
+}
+
+cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off, const int32_t* lengths, int B,
+                              cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    return launch_pdl(zero_slack_kernel, dim3(B), dim3(256), 0, s, kv, ldkv, rec_row_off, lengths);
 }
 
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s) {

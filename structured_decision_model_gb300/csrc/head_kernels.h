@@ -68,6 +68,10 @@ struct FoldArgs {
 cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpad, int H, const int32_t* tile_rec,
                              const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,
                              cudaStream_t s);
+cudaError_t launch_row_stats_rows(const uint16_t* rows, int64_t row_stride, int H, int n, float* mu, float* rstd,
+                                  cudaStream_t s);
+cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off, const int32_t* lengths, int B,
+                              cudaStream_t s);
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s);
 cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
                               uint16_t* out_bf16, float* out_f32, cudaStream_t s);

@@ -94,5 +94,24 @@ class ClefHead:
                             ws.numel(), debug=debug, stream=stream_handle(stream), check=check)
         return out
 
+    def stream_begin(self, schema: B.Schema, stream=None):
+        ws = self.workspace(schema)
+        B.clef_stream_begin(self.cfg, schema, ws.data_ptr(), ws.numel(), stream_handle(stream))
+
+    def stream_rows(self, schema: B.Schema, hidden: torch.Tensor, record: int, row0: int, n_rows: int, stream=None):
+        ws = self._ws
+        B.clef_stream_rows(self.cfg, self.prepared.data_ptr(), schema, hidden.data_ptr(), record, row0, n_rows,
+                           ws.data_ptr(), ws.numel(), stream_handle(stream))
+
+    def stream_finish(self, schema: B.Schema, hidden: torch.Tensor, token_ids: torch.Tensor, lexical: torch.Tensor,
+                      out: Optional[Outputs] = None, debug=None, stream=None) -> Outputs:
+        ws = self._ws
+        out = out if out is not None else self.alloc_outputs(schema)
+        B.clef_stream_finish(self.cfg, self.weight_ptrs, self.prepared.data_ptr(), schema, hidden.data_ptr(),
+                             token_ids.data_ptr(), lexical.data_ptr(), out.logits.data_ptr(), out.probs.data_ptr(),
+                             out.q_value.data_ptr(), out.q_conf.data_ptr(), out.q_argmax.data_ptr(), ws.data_ptr(),
+                             ws.numel(), debug=debug, stream=stream_handle(stream))
+        return out
+
     def device_status(self, stream=None) -> int:
         return B.clef_device_status(self._ws.data_ptr(), stream_handle(stream))

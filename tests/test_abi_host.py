@@ -166,3 +166,20 @@ def test_gemm_entry_validation():
     assert lib.clef_gemm_bf16(p, 64, p, 64, None, p, 64, 10, 48, 64, ctypes.addressof(flags), None) == 1  # N % 64
     assert lib.clef_gemm_bf16(p, 60, p, 64, None, p, 64, 10, 64, 64, ctypes.addressof(flags), None) == 1  # lda
     assert lib.clef_gemm_bf16(0, 64, p, 64, None, p, 64, 10, 64, 64, ctypes.addressof(flags), None) == 1
+
+
+def test_stream_rows_rejects_bad_ranges(small_batch):
+    """Row ranges outside a record are rejected before anything is launched."""
+    bt = small_batch
+    cfg = B.make_config(H=256, vocab=1000)
+    sch = _schema(bt)
+    lib = B.load()
+    args = lambda rec, r0, n: (ctypes.byref(cfg), 1 << 20, ctypes.byref(sch.struct), 1 << 21, rec, r0, n, 1 << 24,
+                               1 << 40, None)
+    L0 = int(bt.lengths[0])
+    assert lib.clef_stream_rows(*args(-1, 0, 64)) == 1
+    assert lib.clef_stream_rows(*args(bt.B, 0, 64)) == 1
+    assert lib.clef_stream_rows(*args(0, -1, 64)) == 1
+    assert lib.clef_stream_rows(*args(0, 0, 0)) == 1
+    assert lib.clef_stream_rows(*args(0, L0 - 10, 11)) == 1
+    assert lib.clef_stream_begin(ctypes.byref(cfg), ctypes.byref(sch.struct), 1 << 24, 1024, None) == 2
