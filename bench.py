@@ -38,7 +38,7 @@ METRIC = "head records/s & memory tokens/s (16K ctx, batch 8); % of BF16 TC / HB
 WORKLOAD = "batch8_l16k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum of one full K/V-projection launch of this
-# workload, scaled from the 2-record ncu capture in profiles/kv_gemm_tcgen05_batch8_l16k.md
+# workload: an ncu capture of the same kernel on the first 2 records, scaled to 8 records
 # (set to None whenever the kernel changes until it is captured again).
 KV_GEMM_TRAFFIC_BYTES = 2.089e9
 

@@ -15,10 +15,12 @@ Sources (web pages, cited by title and section):
   [tuning]       "Clef-Flash inference tuning checklist" (gsyq.cn), tip 1 (batches
                  are padded to the longest record).
 
-Where the pages leave a step open, this file follows the readings listed in the
-repository's design document (pre-LN layers, exact GELU, biases on every Linear,
-eps 1e-5, option-summary by learned attention pooling, prior cosine in the
-backbone space, right padding, ...).  Each function names the readings it uses.
+Where the pages leave a step open, each function states the reading it follows:
+pre-LN layers, exact GELU, biases on every Linear (one summed bias for the three
+option-query and for the three field projections), eps 1e-5, the option summary as a
+learned attention pooling, the prior cosine in the backbone space on the raw pooled
+vectors, right padding, a 4D -> D -> 1 scorer MLP, one learned gate and one learned
+joint scale.
 
 All arithmetic is fp64; bf16 inputs and weights are widened exactly.
 """
