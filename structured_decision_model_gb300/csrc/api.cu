@@ -220,15 +220,13 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
 }
 
 struct WsLayout {
-    size_t flags, split_counters, split_partial, plan, mu, rstd, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf,
+    size_t flags, plan, mu, rstd, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf,
         q_buf, attn_buf, hid_buf, o_hat, f_res, f_hat, z, pm, pl, pacc, total;
     WsLayout(const clef_config* c, const Plan& p) {
         const size_t H = c->hidden, D = c->width, F = c->ffn, NKV = size_t(2) * c->n_route * D;
         const size_t B = p.B, Q = p.Q, O = p.O, R = p.R, MQO = std::max(Q, O);
         Carve cv;
         flags = cv.take(256);
-        split_counters = cv.take(size_t(4) * kSplitSlots * 4);
-        split_partial = cv.take(kSplitPartialBytes);
         plan = cv.take(p.blob.size() * 4);
         mu = cv.take(R * 4);
         rstd = cv.take(R * 4);
@@ -275,17 +273,11 @@ inline cudaError_t mark(const clef_debug_outputs* d, int slot, cudaStream_t st) 
     return cudaEventRecord(static_cast<cudaEvent_t>(d->events[slot]), st);
 }
 
-struct SplitScratch {
-    float* partial = nullptr;
-    int* counters = nullptr;
-};
-
-// Dense GEMM helper: A [M][K] (lda), weight [N][K]; split-K when `sk` is given.
+// Dense GEMM helper: A [M][K] (lda), weight [N][K]; K may be split across a cluster.
 cudaError_t dense(const uint16_t* A, int64_t lda, int M, const uint16_t* Bw, int N, int K, const GemmEpilogue& e,
-                  int* flags, cudaStream_t st, const SplitScratch& sk = SplitScratch()) {
+                  int* flags, cudaStream_t st) {
     GemmProblem g;
-    g.split_partial = sk.partial;
-    g.split_counters = sk.counters;
+    g.allow_split = true;
     g.A = A;
     g.lda = lda;
     g.a_rows = M;
@@ -421,9 +413,6 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     const uint8_t* pw = static_cast<const uint8_t*>(prepared);
     const PreparedLayout PL(cfg);
     int* flags = reinterpret_cast<int*>(ws + L.flags);
-    SplitScratch sk;
-    sk.partial = reinterpret_cast<float*>(ws + L.split_partial);
-    sk.counters = reinterpret_cast<int*>(ws + L.split_counters);
     const int32_t* plan = reinterpret_cast<const int32_t*>(ws + L.plan);
     const int H = cfg->hidden, D = cfg->width, F = cfg->ffn, NKV = 2 * cfg->n_route * D;
     const int B = p.B, Q = p.Q, O = p.O;
@@ -432,9 +421,6 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         const int u = upload_plan(p, ws, ws + L.plan, st);
         if (u != CLEF_OK) return u;
     }
-    // split-K arrival counters start every call at zero (a kernel that stopped on a
-    // timeout may have left some behind)
-    CK(cudaMemsetAsync(sk.counters, 0, size_t(4) * kSplitSlots * 4, st));
     auto T = [&](size_t off) { return plan + off; };
     float* mu = reinterpret_cast<float*>(ws + L.mu);
     float* rstd = reinterpret_cast<float*>(ws + L.rstd);
@@ -482,7 +468,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     {
         GemmEpilogue e;
         e.kind = EPI_F32; e.bias_bf16 = W(weights, 5); e.out = o_res; e.ldo = D;
-        CK(dense(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, e, flags, st, sk)); CK(tick());
+        CK(dense(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, e, flags, st)); CK(tick());
     }
     // 4. memory K/V of every routing layer (LayerNorm folded), real rows only
     if (mode == kForwardAfterStream) {
@@ -516,7 +502,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 0)), W(weights, wi.route(l, 1)), ln_buf, nullptr, st)); CK(tick());
         GemmEpilogue eq;
         eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.route(l, 3)); eq.out = q_buf; eq.ldo = D;
-        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 2)), D, D, eq, flags, st, sk)); CK(tick());
+        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 2)), D, D, eq, flags, st)); CK(tick());
         ra.k_col = 2 * l * D;
         ra.v_col = (2 * l + 1) * D;
         if (l == 0) CK(mark(debug, 2, st));
@@ -525,15 +511,15 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         CK(launch_route_attn_merge(ra, O, st)); CK(tick());
         GemmEpilogue eo;
         eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.route(l, 9)); eo.out = o_res; eo.ldo = D;
-        CK(dense(attn_buf, D, O, W(weights, wi.route(l, 8)), D, D, eo, flags, st, sk)); CK(tick());
+        CK(dense(attn_buf, D, O, W(weights, wi.route(l, 8)), D, D, eo, flags, st)); CK(tick());
         CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 10)), W(weights, wi.route(l, 11)), ln_buf, nullptr,
                              st)); CK(tick());
         GemmEpilogue e1;
         e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.route(l, 13)); e1.out = hid_buf; e1.ldo = F;
-        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 12)), F, D, e1, flags, st, sk)); CK(tick());
+        CK(dense(ln_buf, D, O, W(weights, wi.route(l, 12)), F, D, e1, flags, st)); CK(tick());
         GemmEpilogue e2;
         e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.route(l, 15)); e2.out = o_res; e2.ldo = D;
-        CK(dense(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, e2, flags, st, sk)); CK(tick());
+        CK(dense(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, e2, flags, st)); CK(tick());
     }
     CK(launch_layer_norm(o_res, O, D, W(weights, wi.mid(0)), W(weights, wi.mid(1)), nullptr, o_hat, st)); CK(tick());
     // 6. fields: [u | g | summary] [W_fu | W_fg | W_fs]^T + b + type embedding
@@ -543,25 +529,25 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         GemmEpilogue e;
         e.kind = EPI_F32; e.bias_bf16 = W(weights, wi.mid(7)); e.row_table = W(weights, wi.mid(8));
         e.row_idx = T(p.q_type); e.ld_table = D; e.out = f_res; e.ldo = D;
-        CK(dense(a_field, ld_field, Q, reinterpret_cast<const uint16_t*>(pw + PL.wfield), D, ld_field, e, flags, st, sk)); CK(tick());
+        CK(dense(a_field, ld_field, Q, reinterpret_cast<const uint16_t*>(pw + PL.wfield), D, ld_field, e, flags, st)); CK(tick());
     }
     // 7. joint layers over each record's fields
     for (int i = 0; i < cfg->n_joint; ++i) {
         CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 0)), W(weights, wi.joint(i, 1)), ln_buf, nullptr, st)); CK(tick());
         GemmEpilogue eq;
         eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.joint(i, 3)); eq.out = q_buf; eq.ldo = 3 * D;
-        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 2)), 3 * D, D, eq, flags, st, sk)); CK(tick());
+        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 2)), 3 * D, D, eq, flags, st)); CK(tick());
         CK(launch_field_attn(q_buf, D, cfg->heads, T(p.rec_q_off), B, 0.125f, attn_buf, st)); CK(tick());
         GemmEpilogue eo;
         eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.joint(i, 5)); eo.out = f_res; eo.ldo = D;
-        CK(dense(attn_buf, D, Q, W(weights, wi.joint(i, 4)), D, D, eo, flags, st, sk)); CK(tick());
+        CK(dense(attn_buf, D, Q, W(weights, wi.joint(i, 4)), D, D, eo, flags, st)); CK(tick());
         CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 6)), W(weights, wi.joint(i, 7)), ln_buf, nullptr, st)); CK(tick());
         GemmEpilogue e1;
         e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.joint(i, 9)); e1.out = hid_buf; e1.ldo = F;
-        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 8)), F, D, e1, flags, st, sk)); CK(tick());
+        CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 8)), F, D, e1, flags, st)); CK(tick());
         GemmEpilogue e2;
         e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.joint(i, 11)); e2.out = f_res; e2.ldo = D;
-        CK(dense(hid_buf, F, Q, W(weights, wi.joint(i, 10)), D, F, e2, flags, st, sk)); CK(tick());
+        CK(dense(hid_buf, F, Q, W(weights, wi.joint(i, 10)), D, F, e2, flags, st)); CK(tick());
     }
     CK(launch_layer_norm(f_res, Q, D, W(weights, wi.tail(0)), W(weights, wi.tail(1)), nullptr, f_hat, st)); CK(tick());
     // 8. scorer MLP hidden layer, then scores, softmax and answers
@@ -569,7 +555,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     {
         GemmEpilogue e;
         e.kind = EPI_BF16; e.gelu = 1; e.bias_bf16 = W(weights, wi.tail(5)); e.out = hid_buf; e.ldo = D;
-        CK(dense(z, 4 * D, O, W(weights, wi.tail(4)), D, 4 * D, e, flags, st, sk)); CK(tick());
+        CK(dense(z, 4 * D, O, W(weights, wi.tail(4)), D, 4 * D, e, flags, st)); CK(tick());
     }
     ScoreArgs sc{};
     sc.H = H; sc.D = D; sc.q_rec = T(p.q_rec); sc.q_type = T(p.q_type); sc.q_opt_off = T(p.q_opt_off);

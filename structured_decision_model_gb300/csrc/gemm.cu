@@ -11,6 +11,11 @@
 // accumulators let the epilogue of one tile overlap the mainloop of the next.
 // Operand tiles are 64-element K slices with the 128-byte swizzle.  Tiles are
 // visited N-fastest so that CTAs working at the same time share A tiles in L2.
+// Small-M projections whose tiles cannot fill the GPU split K: the S parts of one
+// output tile run as one thread-block cluster, each stages its fp32 accumulator in
+// its own shared memory, and after a cluster barrier CTA rank r sums rows
+// [r*128/S, (r+1)*128/S) of all S staged tiles in split order through distributed
+// shared memory (deterministic, no global scratch, no CTA waits on a flag).
 // Every mbarrier wait is bounded: on a timeout the CTA sets the timeout flag,
 // waits (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
@@ -27,14 +32,14 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
+constexpr int kMaxSplits = 8;  // cluster size of a split-K tile (portable limit)
 
 struct GemmArgs {
     int n_mtiles, n_ntiles, kblocks;
-    int splits, kb_per_split;      // split-K: each output tile's K range cut into `splits` parts
+    int splits, kb_per_split;      // split-K: each output tile's K range cut into `splits` parts,
+                                   // one cluster of `splits` CTAs per output tile
     const int32_t* a_row_of_mtile;
     GemmEpilogue epi;
-    float* partial;                // [tiles * splits][BM][BN] fp32 partial tiles (splits > 1)
-    int* counters;                 // [tiles][4] arrival counters, zero between launches (splits > 1)
     int* dev_flags;
 };
 
@@ -126,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args) {
     using C = GemmCfg<BN>;
+    constexpr int kRedLd = BN + 4;  // staged split-K row stride (floats): conflict-free float4 rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -270,11 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&tempty[acc]);
                 continue;
             }
-            // split-K: park this split's fp32 rows, count arrivals per (output tile, warp
-            // quarter); the warp whose arrival completes the count sums every split in
-            // split order (deterministic) and runs the epilogue for its 32 rows.  No
-            // warp waits for another.
-            float* mine = args.partial + (int64_t(id.out) * args.splits + id.sp) * (BM * BN) + r_in_tile * BN;
+            // split-K: stage this split's fp32 rows in shared memory.  The operand stages
+            // are idle by now: a split CTA has one tile, whose MMAs have all completed.
+            float* red = reinterpret_cast<float*>(smem) + r_in_tile * kRedLd;
 #pragma unroll 1
             for (int c = 0; c < BN / 16; ++c) {
                 uint32_t r[16];
@@ -282,41 +286,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    __stcg(reinterpret_cast<float4*>(mine + c * 16) + q,
-                           make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                    *reinterpret_cast<float4*>(red + c * 16 + 4 * q) =
+                        make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);  // TMEM is free again; the rest works from global memory
-            __threadfence();
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) last = atomicAdd(args.counters + id.out * 4 + quarter, 1) == args.splits - 1;
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                __threadfence();
-                const float* base = args.partial + int64_t(id.out) * args.splits * (BM * BN) + r_in_tile * BN;
+            mbar_arrive(&tempty[acc]);
+        }
+    }
+    if (args.splits > 1) {
+        // every thread of every CTA of the cluster passes both barriers, on every path
+        cluster_sync();
+        if (warp >= 2) {
+            const TileId id = decode_tile(args, blockIdx.x);
+            const int S = args.splits, rows = BM / S;
+            constexpr int chunks = BN / 16;
+            const uint32_t red0 = smem_u32(smem);
 #pragma unroll 1
-                for (int c = 0; c < BN / 16; ++c) {
-                    float v[16];
+            for (int i = threadIdx.x - 64; i < rows * chunks; i += 128) {
+                const int row = id.sp * rows + i / chunks, c = i % chunks;
+                const uint32_t off = red0 + uint32_t((row * kRedLd + c * 16) * 4);
+                float v[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                    for (int sp = 0; sp < args.splits; ++sp) {
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) {
+                    if (sp < S) {
+                        const uint32_t a = cluster_map(off, uint32_t(sp));
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float4 w =
-                                __ldcg(reinterpret_cast<const float4*>(base + int64_t(sp) * (BM * BN) + c * 16) + q);
+                            const float4 w = ld_cluster_f4(a + 16u * q);
                             v[4 * q] += w.x; v[4 * q + 1] += w.y; v[4 * q + 2] += w.z; v[4 * q + 3] += w.w;
                         }
                     }
+                }
+                const int m = id.mt * BM + row;
+                if (m < args.epi.M) {
                     uint32_t r[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(v[j]);
-                    if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r);
+                    epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r);
                 }
-                if (lane == 0) args.counters[id.out * 4 + quarter] = 0;  // ready for the next launch
             }
         }
+        cluster_sync();  // no CTA leaves while another may still read its shared memory
     }
     __syncthreads();
     if (warp == 1) {
@@ -362,6 +375,36 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 namespace {
 
+// Largest cluster size S (power of two, at most kMaxSplits) of which the GPU can hold
+// at least one cluster of this kernel.
+template <int BN>
+int max_cluster_splits() {
+    static std::once_flag once;
+    static int best = 1;
+    std::call_once(once, [] {
+        for (int S = kMaxSplits; S > 1; S >>= 1) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = S;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(S);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = GemmCfg<BN>::SMEM;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN>, &cfg) == cudaSuccess && n > 0) {
+                best = S;
+                break;
+            }
+        }
+        cudaGetLastError();
+    });
+    return best;
+}
+
 template <int BN>
 cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s) {
     using C = GemmCfg<BN>;
@@ -382,23 +425,39 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     a.kb_per_split = a.kblocks;
     a.a_row_of_mtile = p.a_row_of_mtile;
     a.epi = e;
-    a.partial = p.split_partial;
-    a.counters = p.split_counters;
     a.dev_flags = flags;
     const int sms = num_sms();
     const int out_tiles = a.n_mtiles * a.n_ntiles;
-    if (p.split_partial && p.split_counters && out_tiles < sms && a.kblocks >= 8) {
-        // cut K so that about one wave of CTAs is busy, at least 4 K blocks per split
-        int want = std::min(std::min(sms / out_tiles, a.kblocks / 4), kMaxSplits);
-        want = std::min(want, kSplitSlots / out_tiles);
-        if (want > 1) {
-            a.kb_per_split = (a.kblocks + want - 1) / want;
-            a.splits = (a.kblocks + a.kb_per_split - 1) / a.kb_per_split;
-        }
+    if (p.allow_split && out_tiles < sms && a.kblocks >= 8) {
+        // cut K so that about one wave of CTAs is busy, at least 4 K blocks per split;
+        // S is a power of two that divides the K blocks (every split has work)
+        const int cap = std::min(std::min(sms / out_tiles, a.kblocks / 4), max_cluster_splits<BN>());
+        int S = 1;
+        while (2 * S <= cap && a.kblocks % (2 * S) == 0) S *= 2;
+        a.splits = S;
+        a.kb_per_split = a.kblocks / S;
     }
     const int tiles = out_tiles * a.splits;
-    const int grid = tiles < sms ? tiles : sms;
-    return launch_pdl(gemm_tc_kernel<BN>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, a);
+    if (a.splits == 1) {
+        const int grid = tiles < sms ? tiles : sms;
+        return launch_pdl(gemm_tc_kernel<BN>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, a);
+    }
+    // one CTA per (output tile, split); the splits of a tile form one cluster
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = a.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return counted(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, ta, tb, a));
 }
 
 }  // namespace

@@ -70,15 +70,10 @@ struct GemmProblem {
     int N = 0, K = 0;
     int n_mtiles = 0;                        // 128-row output tiles
     const int32_t* a_row_of_mtile = nullptr; // device [n_mtiles]: first A row of each tile (null: 128 * tile)
-    // split-K scratch (both null: no split).  Partial tiles: kSplitSlots x 128 x 256 fp32;
-    // counters: 4 x kSplitSlots ints that are zero before the launch (the kernel leaves them zero).
-    float* split_partial = nullptr;
-    int* split_counters = nullptr;
+    // split K across a thread-block cluster when the output tiles cannot fill the GPU
+    // (needs no scratch: the partial tiles are summed in distributed shared memory)
+    bool allow_split = false;
 };
-
-constexpr int kMaxSplits = 16;    // K parts per output tile
-constexpr int kSplitSlots = 160;  // output tiles x splits of one split-K launch, at most
-constexpr size_t kSplitPartialBytes = size_t(kSplitSlots) * 128 * 256 * 4;
 
 int num_sms();
 

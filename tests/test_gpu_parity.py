@@ -222,3 +222,45 @@ def test_repeat_calls_are_deterministic():
     b = run_gpu(head, bt, inputs=inputs)
     for k in a:
         np.testing.assert_array_equal(a[k], b[k])
+
+
+# ------------------------------------------------------------ maximum sizes
+
+def test_maximum_questions_and_options():
+    """48 questions in one record (the field-attention limit) and a 256-option question."""
+    rng = np.random.default_rng(17)
+    L = 3000
+    base = synth.make_batch(synth.BatchSpec(name="max", B=2, lengths=[L, 900], questions=(1, 1), options=(2, 2)),
+                            seed=17)
+    # record 0: 48 questions; question 0 has 256 one-row options, the others 2-3 options
+    q_span, o_span, q_type, q_rec, off = [], [], [], [], [0]
+    pos = 40
+    for q in range(48):
+        n = 256 if q == 0 else int(rng.integers(2, 4))
+        q_span.append((pos, pos + 3)); pos += 4
+        for _ in range(n):
+            o_span.append((pos, pos + 1)); pos += 1
+        q_type.append(1 if q % 3 else (2 if q else 1))
+        q_rec.append(0)
+        off.append(len(o_span))
+    assert pos < L
+    q_span.append((100, 110)); o_span += [(200, 205), (300, 302)]; q_type.append(0); q_rec.append(1)
+    off.append(len(o_span))
+    bt = dataclasses.replace(base, q_rec=np.array(q_rec, np.int32), q_type=np.array(q_type, np.int32),
+                             q_span=np.array(q_span, np.int32), q_opt_off=np.array(off, np.int32),
+                             o_span=np.array(o_span, np.int32))
+    head, w = head_for(FULL)
+    compare(run_gpu(head, bt), run_oracle(w, FULL, bt), bt)
+
+
+def test_too_many_questions_is_unsupported():
+    bt = synth.make_batch(synth.BatchSpec(name="max2", B=1, lengths=[2000], questions=(1, 1), options=(2, 2)), seed=18)
+    n = 49
+    bt = dataclasses.replace(bt, q_rec=np.zeros(n, np.int32), q_type=np.ones(n, np.int32),
+                             q_span=np.array([(40 + 4 * q, 42 + 4 * q) for q in range(n)], np.int32),
+                             q_opt_off=np.arange(0, 2 * n + 1, 2).astype(np.int32),
+                             o_span=np.array([(500 + k, 501 + k) for k in range(2 * n)], np.int32))
+    cfg = B.make_config()
+    with pytest.raises(B.ClefError) as e:
+        B.clef_workspace_size(cfg, schema_of(bt))
+    assert e.value.status == 3
