@@ -36,6 +36,7 @@ constexpr int kMaxSplits = 8;  // cluster size of a split-K tile (portable limit
 
 struct GemmArgs {
     int n_mtiles, n_ntiles, kblocks;
+    int a_rows;                    // rows of A's tensor map (a row at or past it reads as zeros)
     int splits, kb_per_split;      // split-K: each output tile's K range cut into `splits` parts,
                                    // one cluster of `splits` CTAs per output tile
     const int32_t* a_row_of_mtile;
@@ -54,6 +55,28 @@ __device__ __forceinline__ TileId decode_tile(const GemmArgs& a, int t) {
     id.mt = id.out / a.n_ntiles;
     id.nt = id.out % a.n_ntiles;
     return id;
+}
+
+// The it-th tile of this CTA's persistent walk.  MC == 1: tiles t = blockIdx.x + it *
+// gridDim.x.  MC > 1: the CTAs of a cluster take MC consecutive M tiles of one N tile
+// (rank r takes M tile MC * group + r) and walk the groups together, so that each can
+// multicast its 1/MC share of the common B tile to all of them.
+template <int MC>
+__device__ __forceinline__ bool tile_at(const GemmArgs& a, int it, TileId& id) {
+    if constexpr (MC == 1) {
+        const int t = int(blockIdx.x) + it * int(gridDim.x);
+        if (t >= a.n_mtiles * a.n_ntiles * a.splits) return false;
+        id = decode_tile(a, t);
+        return true;
+    } else {
+        const int g = int(blockIdx.x) / MC + it * (int(gridDim.x) / MC);
+        if (g >= (a.n_mtiles + MC - 1) / MC * a.n_ntiles) return false;
+        id.sp = 0;
+        id.nt = g % a.n_ntiles;
+        id.mt = (g / a.n_ntiles) * MC + int(blockIdx.x) % MC;
+        id.out = id.mt * a.n_ntiles + id.nt;
+        return true;
+    }
 }
 
 template <int BN>
@@ -126,11 +149,13 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int
     }
 }
 
-template <int BN>
+// MC > 1 (B multicast across an M-cluster) is only launched without split-K.
+template <int BN, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap tmBp, const GemmArgs args) {
     using C = GemmCfg<BN>;
+    constexpr uint16_t kPeers = uint16_t((1u << MC) - 1u);  // multicast mask: every CTA of the cluster
     constexpr int kRedLd = BN + 4;  // staged split-K row stride (floats): conflict-free float4 rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -148,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], MC);  // one MMA commit from each CTA that reads the stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -160,19 +185,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+        prefetch_tensormap(MC > 1 ? &tmBp : &tmB);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tc_fence_before();
     }
     __syncthreads();
+    // peers multicast into this CTA's stages and arrive on its barriers: all barriers of
+    // the cluster are initialised before anyone issues a copy
+    if constexpr (MC > 1) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     griddep_launch();
     griddep_wait();  // operands and outputs may belong to the previous kernel of the stream
 
-    const int n_tiles = args.n_mtiles * args.n_ntiles * args.splits;
     const int kblocks = args.kblocks;
 
     if (warp == 0) {
@@ -182,9 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t armed[C::STAGES];
             for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const TileId id = decode_tile(args, tile);
-                const int a_row = args.a_row_of_mtile ? args.a_row_of_mtile[id.mt] : id.mt * BM;
+            TileId id;
+            for (int it = 0; ok && tile_at<MC>(args, it, id); ++it) {
+                const int a_row = id.mt >= args.n_mtiles ? args.a_rows
+                                  : args.a_row_of_mtile ? args.a_row_of_mtile[id.mt] : id.mt * BM;
                 const int b_row = id.nt * BN;
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -194,7 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
                     tma_load_2d(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, &full[stage]);
-                    tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
+                    if constexpr (MC == 1) {
+                        tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
+                    } else {
+                        const int r = int(blockIdx.x) % MC;
+                        tma_load_2d_mc(sB + stage * C::B_BYTES + r * (C::B_BYTES / MC), &tmBp, kb * BK,
+                                       b_row + r * (BN / MC), &full[stage], kPeers);
+                    }
                     ++armed[stage];
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -215,13 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
+            TileId id;
+            for (int it = 0; ok && tile_at<MC>(args, it, id); ++it, ++local) {
                 const int acc = local & 1;
                 const uint32_t use = uint32_t(local >> 1);
                 if (!mbar_wait_bounded(&tempty[acc], (use & 1u) ^ 1u, abort_flag, args.dev_flags)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-                const TileId id = decode_tile(args, tile);
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.dev_flags)) {
@@ -236,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
                                     (kb > kb0 || k > 0) ? 1u : 0u);
                     }
-                    tc_commit(&empty[stage]);
+                    if constexpr (MC == 1) tc_commit(&empty[stage]);
+                    else tc_commit_mc(&empty[stage], kPeers);  // the stage is free once every CTA is done
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -253,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;  // TMEM lanes this warp may read
         const int r_in_tile = quarter * 32 + lane;
         int local = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+        TileId id;
+        for (int it = 0; tile_at<MC>(args, it, id); ++it, ++local) {
             const int acc = local & 1;
             const uint32_t use = uint32_t(local >> 1);
             int ok = 1;
@@ -261,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const TileId id = decode_tile(args, tile);
             const int m = id.mt * BM + r_in_tile;
             const bool store = m < args.epi.M;
             if (args.splits == 1) {
@@ -332,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // no CTA leaves while another may still read its shared memory
     }
     __syncthreads();
+    // no CTA leaves while a peer may still multicast into it or arrive on its barriers
+    if constexpr (MC > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -375,6 +412,41 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 namespace {
 
+// Opts the kernel into its dynamic shared memory size (once per instantiation).
+template <int BN, int MC>
+cudaError_t kernel_attributes() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   GemmCfg<BN>::SMEM);
+    });
+    return err;
+}
+
+// How many clusters of `size` CTAs of this kernel the GPU holds at once (0: none).
+template <int BN, int MC>
+int active_clusters(int size) {
+    if (kernel_attributes<BN, MC>() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(size);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = GemmCfg<BN>::SMEM;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, MC>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // Largest cluster size S (power of two, at most kMaxSplits) of which the GPU can hold
 // at least one cluster of this kernel.
 template <int BN>
@@ -383,36 +455,47 @@ int max_cluster_splits() {
     static int best = 1;
     std::call_once(once, [] {
         for (int S = kMaxSplits; S > 1; S >>= 1) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = S;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(S);
-            cfg.blockDim = dim3(kThreads);
-            cfg.dynamicSmemBytes = GemmCfg<BN>::SMEM;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN>, &cfg) == cudaSuccess && n > 0) {
+            if (active_clusters<BN, 1>(S) > 0) {
                 best = S;
                 break;
             }
         }
-        cudaGetLastError();
     });
     return best;
 }
 
-template <int BN>
-cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s) {
-    using C = GemmCfg<BN>;
+// Clusters of two B-multicast CTAs the GPU holds at once (0: the mode is unavailable).
+int multicast_pairs() {
     static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    });
+    static int n = 0;
+    std::call_once(once, [] { n = active_clusters<256, 2>(2); });
+    return n;
+}
+
+cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs), int grid, int cluster,
+                           size_t smem, cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const CUtensorMap& tbp, const GemmArgs& a) {
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return counted(cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbp, a));
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s, int splits) {
+    using C = GemmCfg<BN>;
+    const cudaError_t attr_err = kernel_attributes<BN, 1>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ta, tb;
     if (!make_tma_2d_bf16(&ta, p.A, uint64_t(p.K), uint64_t(p.a_rows), uint64_t(p.lda), BM)) return cudaErrorInvalidValue;
@@ -421,43 +504,33 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     a.n_mtiles = p.n_mtiles;
     a.n_ntiles = p.N / BN;
     a.kblocks = p.K / BK;
-    a.splits = 1;
-    a.kb_per_split = a.kblocks;
+    a.a_rows = int(p.a_rows);
+    a.splits = splits;
+    a.kb_per_split = a.kblocks / splits;
     a.a_row_of_mtile = p.a_row_of_mtile;
     a.epi = e;
     a.dev_flags = flags;
     const int sms = num_sms();
     const int out_tiles = a.n_mtiles * a.n_ntiles;
-    if (p.allow_split && out_tiles < sms && a.kblocks >= 8) {
-        // cut K so that about one wave of CTAs is busy, at least 4 K blocks per split;
-        // S is a power of two that divides the K blocks (every split has work)
-        const int cap = std::min(std::min(sms / out_tiles, a.kblocks / 4), max_cluster_splits<BN>());
-        int S = 1;
-        while (2 * S <= cap && a.kblocks % (2 * S) == 0) S *= 2;
-        a.splits = S;
-        a.kb_per_split = a.kblocks / S;
-    }
     const int tiles = out_tiles * a.splits;
-    if (a.splits == 1) {
-        const int grid = tiles < sms ? tiles : sms;
-        return launch_pdl(gemm_tc_kernel<BN>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, a);
+    if (a.splits > 1)  // one CTA per (output tile, split); the splits of a tile form one cluster
+        return launch_cluster(gemm_tc_kernel<BN, 1>, tiles, a.splits, C::SMEM, s, ta, tb, tb, a);
+    if constexpr (BN == 256) {
+        // Operand-heavy launches (more tiles than SMs): pairs of CTAs on neighbouring M
+        // tiles share each B tile, every CTA loading half of it for both, which cuts the
+        // L2-to-SM operand traffic by a third.
+        const int pairs = out_tiles > sms ? multicast_pairs() : 0;
+        if (pairs > 0 && kernel_attributes<BN, 2>() == cudaSuccess) {
+            CUtensorMap tbp;
+            if (!make_tma_2d_bf16(&tbp, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN / 2))
+                return cudaErrorInvalidValue;
+            const int groups = (a.n_mtiles + 1) / 2 * a.n_ntiles;
+            const int grid = 2 * std::min(groups, pairs);
+            return launch_cluster(gemm_tc_kernel<BN, 2>, grid, 2, C::SMEM, s, ta, tb, tbp, a);
+        }
     }
-    // one CTA per (output tile, split); the splits of a tile form one cluster
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = a.splits;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return counted(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, ta, tb, a));
+    const int grid = tiles < sms ? tiles : sms;
+    return launch_pdl(gemm_tc_kernel<BN, 1>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, tb, a);
 }
 
 }  // namespace
@@ -474,18 +547,44 @@ int num_sms() {
 cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_flags, cudaStream_t s, int force_bn) {
     if (p.n_mtiles <= 0 || p.N <= 0) return cudaSuccess;
     if (p.K % BK != 0 || p.N % 64 != 0 || p.lda % 8 != 0 || p.ldb % 8 != 0) return cudaErrorInvalidValue;
-    int bn = force_bn;
-    if (bn == 0) {
-        const int sms = num_sms();
+    const int sms = num_sms();
+    const int kblocks = p.K / BK;
+    int bn = force_bn, splits = 1;
+    if (bn == 0 && !p.allow_split) {
         bn = 64;
         if (p.N % 256 == 0 && p.n_mtiles * (p.N / 256) >= sms) bn = 256;
         else if (p.N % 128 == 0 && p.n_mtiles * (p.N / 128) >= sms) bn = 128;
+    } else if (bn == 0) {
+        // Small-M projections: pick the tile width and the split count with the least
+        // estimated time.  A launch streams its operand tiles from L2 (aggregate about
+        // 11 TB/s) into CTAs that each take in about 90 GB/s with this pipeline depth;
+        // a split costs about 2 us of cluster barriers and reduction.  The constants
+        // come from sweeping every (width, split) of the head's projections on GB300.
+        double best = 1e30;
+        for (int w : {64, 128, 256}) {
+            if (p.N % w) continue;
+            const int tiles = p.n_mtiles * (p.N / w);
+            const int max_s = w == 64 ? max_cluster_splits<64>() : (w == 128 ? max_cluster_splits<128>()
+                                                                               : max_cluster_splits<256>());
+            for (int S = 1; S <= 4 && S <= max_s; S *= 2) {
+                if (S > 1 && (kblocks % S || kblocks / S < 8 || tiles * S > sms)) continue;
+                const int ctas = std::min(tiles * S, sms);
+                const int waves = (tiles * S + sms - 1) / sms;
+                const double per_cta = double(waves) * (kblocks / S) * (BM + w) * BK * 2.0;
+                const double t = std::max(per_cta / 90e3, per_cta * ctas / 11e6) + (S > 1 ? 2.0 : 0.0);
+                if (t < best) {
+                    best = t;
+                    bn = w;
+                    splits = S;
+                }
+            }
+        }
     }
     if (p.N % bn != 0) return cudaErrorInvalidValue;
     switch (bn) {
-        case 256: return launch_bn<256>(p, e, dev_flags, s);
-        case 128: return launch_bn<128>(p, e, dev_flags, s);
-        default: return launch_bn<64>(p, e, dev_flags, s);
+        case 256: return launch_bn<256>(p, e, dev_flags, s, splits);
+        case 128: return launch_bn<128>(p, e, dev_flags, s, splits);
+        default: return launch_bn<64>(p, e, dev_flags, s, splits);
     }
 }
 

@@ -33,7 +33,8 @@ def _lib():
 # ------------------------------------------------------------------- GEMM
 
 @pytest.mark.parametrize("M,N,K", [(1, 64, 64), (100, 1024, 1024), (129, 256, 512), (300, 4096, 1024),
-                                   (1000, 1024, 4096), (2048, 4096, 4096), (777, 3072, 1024), (64, 1024, 12288)])
+                                   (1000, 1024, 4096), (2048, 4096, 4096), (777, 3072, 1024), (64, 1024, 12288),
+                                   (1300, 4096, 1024)])
 def test_gemm_matches_torch(M, N, K):
     g = torch.Generator(device="cuda").manual_seed(M * 7 + N + K)
     A = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=g).to(torch.bfloat16)
