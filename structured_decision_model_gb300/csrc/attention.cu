@@ -258,18 +258,30 @@ __global__ void __launch_bounds__(256) route_attn_merge_kernel(const RouteAttnAr
     const int o_base = a.rec_o_off[b];
     const int O_b = a.rec_o_off[b + 1] - o_base;
     const int nch = (a.lengths[b] + kAttnChunk - 1) / kAttnChunk;
+    const int64_t p0 = a.rec_part_off[b] + int64_t(h) * O_b + (o - o_base);  // chunk k at p0 + k * heads * O_b
+    const int64_t pstride = int64_t(a.heads) * O_b;
+    // lane k holds chunk k's statistics (32 chunks at a time): one round trip for all of them
     float M = -INFINITY;
-    for (int k = 0; k < nch; ++k)
-        M = fmaxf(M, a.pm[a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base)]);
+    for (int k = lane; k < nch; k += 32) M = fmaxf(M, a.pm[p0 + k * pstride]);
+    M = warp_max(M);
     float Ls = 0.f, x0 = 0.f, x1 = 0.f;
-    for (int k = 0; k < nch; ++k) {
-        const int64_t pi = a.rec_part_off[b] + (int64_t(k) * a.heads + h) * O_b + (o - o_base);
-        const float w = exp2f(a.pm[pi] - M);
-        Ls += a.pl[pi] * w;
-        const float2 v = *reinterpret_cast<const float2*>(a.pacc + pi * 64 + lane * 2);
-        x0 += v.x * w;
-        x1 += v.y * w;
+    for (int k0 = 0; k0 < nch; k0 += 32) {
+        const int k = k0 + lane;
+        float w = 0.f;
+        if (k < nch) {
+            w = exp2f(a.pm[p0 + k * pstride] - M);
+            Ls += a.pl[p0 + k * pstride] * w;
+        }
+        const int nk = min(32, nch - k0);
+#pragma unroll 8
+        for (int j = 0; j < nk; ++j) {  // chunks in order; the weights come from their lanes
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            const float2 v = *reinterpret_cast<const float2*>(a.pacc + (p0 + (k0 + j) * pstride) * 64 + lane * 2);
+            x0 += v.x * wj;
+            x1 += v.y * wj;
+        }
     }
+    Ls = warp_sum(Ls);
     const float inv = 1.0f / Ls;
     *reinterpret_cast<uint32_t*>(a.out + int64_t(o) * a.ldo + h * 64 + lane * 2) = pack_bf16(x0 * inv, x1 * inv);
 }

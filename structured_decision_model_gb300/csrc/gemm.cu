@@ -464,12 +464,25 @@ int max_cluster_splits() {
     return best;
 }
 
-// Clusters of two B-multicast CTAs the GPU holds at once (0: the mode is unavailable).
-int multicast_pairs() {
+// Clusters of MC B-multicast CTAs the GPU holds at once (0: the mode is unavailable).
+template <int MC>
+int multicast_clusters() {
     static std::once_flag once;
     static int n = 0;
-    std::call_once(once, [] { n = active_clusters<256, 2>(2); });
+    std::call_once(once, [] { n = active_clusters<256, MC>(MC); });
     return n;
+}
+
+template <int BN, int MC>
+cudaError_t launch_multicast(const GemmProblem& p, const GemmArgs& a, int clusters, cudaStream_t s,
+                             const CUtensorMap& ta, const CUtensorMap& tb) {
+    if (kernel_attributes<BN, MC>() != cudaSuccess) return cudaErrorInvalidValue;
+    CUtensorMap tbp;
+    if (!make_tma_2d_bf16(&tbp, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN / MC))
+        return cudaErrorInvalidValue;
+    const int groups = (a.n_mtiles + MC - 1) / MC * a.n_ntiles;
+    const int grid = MC * std::min(groups, clusters);
+    return launch_cluster(gemm_tc_kernel<BN, MC>, grid, MC, GemmCfg<BN>::SMEM, s, ta, tb, tbp, a);
 }
 
 cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs), int grid, int cluster,
@@ -519,15 +532,8 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
         // Operand-heavy launches (more tiles than SMs): pairs of CTAs on neighbouring M
         // tiles share each B tile, every CTA loading half of it for both, which cuts the
         // L2-to-SM operand traffic by a third.
-        const int pairs = out_tiles > sms ? multicast_pairs() : 0;
-        if (pairs > 0 && kernel_attributes<BN, 2>() == cudaSuccess) {
-            CUtensorMap tbp;
-            if (!make_tma_2d_bf16(&tbp, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN / 2))
-                return cudaErrorInvalidValue;
-            const int groups = (a.n_mtiles + 1) / 2 * a.n_ntiles;
-            const int grid = 2 * std::min(groups, pairs);
-            return launch_cluster(gemm_tc_kernel<BN, 2>, grid, 2, C::SMEM, s, ta, tb, tbp, a);
-        }
+        const int pairs = out_tiles > sms ? multicast_clusters<2>() : 0;
+        if (pairs > 0) return launch_multicast<BN, 2>(p, a, pairs, s, ta, tb);
     }
     const int grid = tiles < sms ? tiles : sms;
     return launch_pdl(gemm_tc_kernel<BN, 1>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, tb, a);

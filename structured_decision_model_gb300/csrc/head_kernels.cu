@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(256) build_z_kernel(const float* __restrict__ 
 __global__ void __launch_bounds__(256) score_softmax_kernel(ScoreArgs a) {
     griddep_wait();
     griddep_launch();
+    extern __shared__ float4 s_dyn4[];  // u_q + g_b [H], then f_hat_q [D]: read once, used by every option
     __shared__ float s_logit[256];
     __shared__ float s_red[8];
     __shared__ float s_anchor_norm;
@@ -415,15 +416,20 @@ __global__ void __launch_bounds__(256) score_softmax_kernel(ScoreArgs a) {
     const int j0 = a.q_opt_off[q], n = a.q_opt_off[q + 1] - j0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, D = a.D;
-    const float* u = a.u32 + int64_t(q) * H;
-    const float* g = a.g32 + int64_t(b) * H;
-    // |u_q + g_b|
+    const float4* u4 = reinterpret_cast<const float4*>(a.u32 + int64_t(q) * H);
+    const float4* g4 = reinterpret_cast<const float4*>(a.g32 + int64_t(b) * H);
+    const float4* f4 = reinterpret_cast<const float4*>(a.f_hat + int64_t(q) * D);
+    float4* s_ug = s_dyn4;
+    float4* s_f = s_dyn4 + H / 4;
+    // anchor u_q + g_b and its norm
     float ss = 0.f;
     for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
-        const float4 uv = reinterpret_cast<const float4*>(u)[c], gv = reinterpret_cast<const float4*>(g)[c];
-        const float v0 = uv.x + gv.x, v1 = uv.y + gv.y, v2 = uv.z + gv.z, v3 = uv.w + gv.w;
-        ss += v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3;
+        const float4 uv = u4[c], gv = g4[c];
+        const float4 v = make_float4(uv.x + gv.x, uv.y + gv.y, uv.z + gv.z, uv.w + gv.w);
+        s_ug[c] = v;
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
+    for (int c = threadIdx.x; c < D / 4; c += blockDim.x) s_f[c] = f4[c];
     ss = warp_sum(ss);
     if (lane == 0) s_red[warp] = ss;
     __syncthreads();
@@ -435,27 +441,23 @@ __global__ void __launch_bounds__(256) score_softmax_kernel(ScoreArgs a) {
     __syncthreads();
     const float gate = 1.0f / (1.0f + expf(-bf16_to_float(a.gate[0])));
     const float jscale = bf16_to_float(a.joint_scale[0]);
-    const float* f = a.f_hat + int64_t(q) * D;
     for (int jj = warp; jj < n; jj += 8) {
         const int j = j0 + jj;
         const float4* x4 = reinterpret_cast<const float4*>(a.x32 + int64_t(j) * H);
-        const float4* u4 = reinterpret_cast<const float4*>(u);
-        const float4* g4 = reinterpret_cast<const float4*>(g);
         float xa = 0.f, xx = 0.f;
-#pragma unroll 4
+#pragma unroll 8
         for (int c = lane; c < H / 4; c += 32) {
-            const float4 xv = x4[c], uv = u4[c], gv = g4[c];
-            xa += xv.x * (uv.x + gv.x) + xv.y * (uv.y + gv.y) + xv.z * (uv.z + gv.z) + xv.w * (uv.w + gv.w);
+            const float4 xv = x4[c], av = s_ug[c];
+            xa += xv.x * av.x + xv.y * av.y + xv.z * av.z + xv.w * av.w;
             xx += xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
         }
         const float4* o4 = reinterpret_cast<const float4*>(a.o_hat + int64_t(j) * D);
-        const float4* f4 = reinterpret_cast<const float4*>(f);
         const uint2* hm = reinterpret_cast<const uint2*>(a.mlp_hidden + int64_t(j) * D);
         const uint2* w2 = reinterpret_cast<const uint2*>(a.w2);
         float fo = 0.f, ff = 0.f, oo = 0.f, mm = 0.f;
-#pragma unroll 2
+#pragma unroll 8
         for (int c = lane; c < D / 4; c += 32) {
-            const float4 fv = f4[c], ov = o4[c];
+            const float4 fv = s_f[c], ov = o4[c];
             fo += fv.x * ov.x + fv.y * ov.y + fv.z * ov.z + fv.w * ov.w;
             ff += fv.x * fv.x + fv.y * fv.y + fv.z * fv.z + fv.w * fv.w;
             oo += ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w;
@@ -615,7 +617,8 @@ cudaError_t launch_build_z(const float* f_hat, const float* o_hat, const int32_t
 
 cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s) {
     if (Q <= 0) return cudaSuccess;
-    return launch_pdl(score_softmax_kernel, dim3(Q), dim3(256), 0, s, a);
+    const size_t smem = size_t(a.H + a.D) * sizeof(float);  // at most 40 KB for supported widths
+    return launch_pdl(score_softmax_kernel, dim3(Q), dim3(256), smem, s, a);
 }
 
 cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaStream_t s) {
