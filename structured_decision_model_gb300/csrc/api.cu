@@ -64,12 +64,12 @@ struct PreparedLayout {
 
 // Host-built plan of one batch: tables the kernels index, and sizes.
 struct Plan {
-    int B = 0, Q = 0, O = 0, R = 0, n_mtiles = 0, n_items = 0, n_chunks = 0, max_rec_options = 0;
+    int B = 0, Q = 0, O = 0, R = 0, n_mtiles = 0, n_items = 0, n_chunks = 0, n_units = 0, max_rec_options = 0;
     int64_t P = 0;  // attention partial rows
     std::vector<int32_t> blob;  // int32 tables followed by the int64 partial offsets
     // offsets (in int32 units) of each table in the blob
     size_t lengths, rec_row_off, rec_q_off, rec_o_off, q_rec, q_type, q_span, q_opt_off, o_rec, o_q, o_span,
-        tile_rec, tile_a_row, item_kind, item_index, chunk_rec, chunk_idx, rec_part_off;
+        tile_rec, tile_a_row, item_kind, item_index, chunk_rec, chunk_idx, unit_cx, unit_qp, rec_part_off;
 };
 
 int validate_schema(const clef_config* c, const clef_schema* s) {
@@ -205,6 +205,27 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
         for (int b = 0; b < B; ++b) {
             const int n = (s->lengths[b] + kAttnChunk - 1) / kAttnChunk;
             for (int k = 0; k < n; ++k, ++i) { v[p.chunk_rec + i] = b; v[p.chunk_idx + i] = k; }
+        }
+    }
+    // routing-attention work units: (chunk, block of kAttnQRows options of the chunk's
+    // record), chunk-major so that units working at the same time share memory rows
+    {
+        int n = 0;
+        for (int cx = 0; cx < nch; ++cx) {
+            const int b = v[p.chunk_rec + cx];
+            n += (ro[b + 1] - ro[b] + kAttnQRows - 1) / kAttnQRows;
+        }
+        p.n_units = n;
+        p.unit_cx = put(n);
+        p.unit_qp = put(n);
+        int u = 0;
+        for (int cx = 0; cx < nch; ++cx) {
+            const int b = v[p.chunk_rec + cx];
+            const int nq = (ro[b + 1] - ro[b] + kAttnQRows - 1) / kAttnQRows;
+            for (int qp = 0; qp < nq; ++qp, ++u) {
+                v[p.unit_cx + u] = cx;
+                v[p.unit_qp + u] = qp;
+            }
         }
     }
     if (v.size() & 1) put(1);  // 8-byte alignment of the int64 table
@@ -494,6 +515,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     ra.q = q_buf; ra.ldq = D; ra.kv = kv; ra.ldkv = NKV; ra.kv_rows = p.R; ra.heads = cfg->heads; ra.flags = flags;
     ra.scale_log2 = 1.4426950408889634f / 8.0f;
     ra.chunk_rec = T(p.chunk_rec); ra.chunk_idx = T(p.chunk_idx); ra.lengths = T(p.lengths);
+    ra.unit_cx = T(p.unit_cx); ra.unit_qp = T(p.unit_qp); ra.n_units = p.n_units;
     ra.rec_row_off = T(p.rec_row_off); ra.rec_o_off = T(p.rec_o_off);
     ra.rec_part_off = reinterpret_cast<const int64_t*>(T(p.rec_part_off)); ra.o_rec = T(p.o_rec);
     ra.pm = reinterpret_cast<float*>(ws + L.pm); ra.pl = reinterpret_cast<float*>(ws + L.pl);
@@ -506,7 +528,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         ra.k_col = 2 * l * D;
         ra.v_col = (2 * l + 1) * D;
         if (l == 0) CK(mark(debug, 2, st));
-        CK(launch_route_attn_partial(ra, p.n_chunks, O, p.max_rec_options, st)); CK(tick());
+        CK(launch_route_attn_partial(ra, O, st)); CK(tick());
         if (l == 0) CK(mark(debug, 3, st));
         CK(launch_route_attn_merge(ra, O, st)); CK(tick());
         GemmEpilogue eo;

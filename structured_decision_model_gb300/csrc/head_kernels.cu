@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(256) zero_slack_kernel(uint16_t* __restrict__ 
 // rows instead (the bit-exact index check).
 // =====================================================================
 template <bool RAW>
-__global__ void __launch_bounds__(256, 4) span_pool_kernel(SpanPoolArgs a) {
+__global__ void __launch_bounds__(256, 3) span_pool_kernel(SpanPoolArgs a) {
     griddep_wait();
     griddep_launch();
     const int kind = a.item_kind[blockIdx.x];
@@ -133,22 +133,23 @@ __global__ void __launch_bounds__(256, 4) span_pool_kernel(SpanPoolArgs a) {
         float acc[8], lex[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) { acc[k] = 0.f; lex[k] = 0.f; }
-        // rows in groups of 4: all loads of a group are issued before its sums, which are
+        // rows in groups of 6: all loads of a group are issued before its sums, which are
         // then taken in row order (the same order as one row at a time); the hidden rows and
-        // the lexical rows of an option span are two separate passes (fewer live registers)
-        for (int t0 = s; t0 < e; t0 += 4) {
-            const int nr = min(4, e - t0);
-            uint4 w[4];
-            float m[4], rs[4];
+        // the lexical rows of an option span are two separate passes (fewer live registers).
+        // Groups of 6 at 3 CTAs per SM measured fastest (groups of 4, 6, 8 at 2-4 CTAs).
+        for (int t0 = s; t0 < e; t0 += 6) {
+            const int nr = min(6, e - t0);
+            uint4 w[6];
+            float m[6], rs[6];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 6; ++u) {
                 if (u < nr) {
                     w[u] = __ldg(reinterpret_cast<const uint4*>(a.hidden + (rec_base + t0 + u) * a.row_stride) + c8);
                     if (!RAW) { m[u] = a.mu[stat_base + t0 + u]; rs[u] = a.rstd[stat_base + t0 + u]; }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 6; ++u) {
                 if (u < nr) {
                     const float v[8] = {bf16_lo(w[u].x), bf16_hi(w[u].x), bf16_lo(w[u].y), bf16_hi(w[u].y),
                                         bf16_lo(w[u].z), bf16_hi(w[u].z), bf16_lo(w[u].w), bf16_hi(w[u].w)};
@@ -163,11 +164,11 @@ __global__ void __launch_bounds__(256, 4) span_pool_kernel(SpanPoolArgs a) {
             }
         }
         if (kind == 1) {
-            for (int t0 = s; t0 < e; t0 += 4) {
-                const int nr = min(4, e - t0);
-                uint4 x[4];
+            for (int t0 = s; t0 < e; t0 += 6) {
+                const int nr = min(6, e - t0);
+                uint4 x[6];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 6; ++u) {
                     x[u] = make_uint4(0, 0, 0, 0);
                     if (u < nr) {
                         const int id = a.token_ids[rec_base + t0 + u];
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(256, 4) span_pool_kernel(SpanPoolArgs a) {
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 6; ++u) {
                     lex[0] += bf16_lo(x[u].x); lex[1] += bf16_hi(x[u].x);
                     lex[2] += bf16_lo(x[u].y); lex[3] += bf16_hi(x[u].y);
                     lex[4] += bf16_lo(x[u].z); lex[5] += bf16_hi(x[u].z);

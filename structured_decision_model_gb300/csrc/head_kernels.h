@@ -7,6 +7,7 @@
 namespace clef {
 
 constexpr int kAttnChunk = 1024;  // memory rows per split-L routing-attention work item
+constexpr int kAttnQRows = 64;    // option queries per routing-attention work item
 constexpr int kMaxFields = 48;    // questions per record handled by the field self-attention kernel
 constexpr int kMaxOptions = 256;  // options per question
 constexpr int kPlanChunkInts = 4000;  // plan ints carried by one upload launch (16 KB of parameters)
@@ -37,14 +38,15 @@ struct RouteAttnArgs {
     int k_col, v_col;                     // column of this layer's K and V blocks
     int heads;
     float scale_log2;                     // log2(e) / sqrt(head dim)
-    const int32_t* chunk_rec; const int32_t* chunk_idx;
+    const int32_t* chunk_rec; const int32_t* chunk_idx;  // per chunk: record, chunk index in the record
+    const int32_t* unit_cx; const int32_t* unit_qp;      // per work unit: chunk, block of kAttnQRows options
+    int n_units;
     const int32_t* lengths; const int32_t* rec_row_off; const int32_t* rec_o_off;
     const int64_t* rec_part_off;
     const int32_t* o_rec;
     float* pm; float* pl; float* pacc;    // partials
     uint16_t* out; int64_t ldo;           // [O][D] bf16 merged output
     int* flags;                           // device status word
-    int qblocks, n_chunks;                // grid decomposition (set by the launcher)
 };
 
 struct ScoreArgs {
@@ -75,7 +77,7 @@ cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s);
 cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
                               uint16_t* out_bf16, float* out_f32, cudaStream_t s);
-cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int n_chunks, int O, int max_rec_options,
+cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int O,
                                       cudaStream_t s);
 cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s);
 cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,
