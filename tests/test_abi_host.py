@@ -183,3 +183,13 @@ def test_stream_rows_rejects_bad_ranges(small_batch):
     assert lib.clef_stream_rows(*args(0, 0, 0)) == 1
     assert lib.clef_stream_rows(*args(0, L0 - 10, 11)) == 1
     assert lib.clef_stream_begin(ctypes.byref(cfg), ctypes.byref(sch.struct), 1 << 24, 1024, None) == 2
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without the compiled library the binding raises; there is no fallback path."""
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "libclef_head.so"))
+    with pytest.raises(FileNotFoundError):
+        B.load()
+    with pytest.raises(FileNotFoundError):
+        B.clef_weight_count(B.make_config())
