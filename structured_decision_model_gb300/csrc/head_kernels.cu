@@ -250,8 +250,12 @@ __global__ void __launch_bounds__(256, 3) span_pool_kernel(SpanPoolArgs a) {
 
 // =====================================================================
 // LayerNorm of fp32 rows of width D (pre-LN of the routing / joint layers and the
-// final option / field norms).  One warp per row, two-pass statistics.
+// final option / field norms).  Two-pass statistics over the row held in registers.
 // =====================================================================
+// One warp per row; lane l owns the 8-column chunks l, l + 32, ... (NCK of them at
+// most), so the row, the weight and the bias are all loaded with 16-byte accesses in
+// one round trip before the two reductions.
+template <int NCK>
 __global__ void __launch_bounds__(256) layer_norm_kernel(const float* __restrict__ x, int rows, int D,
                                                         const uint16_t* __restrict__ w,
                                                         const uint16_t* __restrict__ bias,
@@ -261,27 +265,59 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const float* __restrict
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + warp;
     if (r >= rows) return;
-    constexpr int kMax = 64;  // D <= 2048
-    float v[kMax];
-    const float* row = x + int64_t(r) * D;
-    const int n = D >> 5;
+    const int nc = D >> 3;  // 8-column chunks in the row
+    const float4* row = reinterpret_cast<const float4*>(x + int64_t(r) * D);
+    float v[NCK][8];
+    uint4 wv[NCK], bv[NCK];
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMax; ++i)
-        if (i < n) { v[i] = row[i * 32 + lane]; s += v[i]; }
+    for (int k = 0; k < NCK; ++k) {
+        const int c = lane + 32 * k;
+        if (c < nc) {
+            const float4 a0 = row[2 * c], a1 = row[2 * c + 1];
+            wv[k] = __ldg(reinterpret_cast<const uint4*>(w) + c);
+            bv[k] = __ldg(reinterpret_cast<const uint4*>(bias) + c);
+            v[k][0] = a0.x; v[k][1] = a0.y; v[k][2] = a0.z; v[k][3] = a0.w;
+            v[k][4] = a1.x; v[k][5] = a1.y; v[k][6] = a1.z; v[k][7] = a1.w;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += v[k][j];
+        }
+    }
     const float m = warp_sum(s) / float(D);
     float q = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMax; ++i)
-        if (i < n) { const float d = v[i] - m; q += d * d; }
+    for (int k = 0; k < NCK; ++k) {
+        if (lane + 32 * k < nc) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float d = v[k][j] - m;
+                q += d * d;
+            }
+        }
+    }
     const float rs = rsqrtf(warp_sum(q) / float(D) + 1e-5f);
 #pragma unroll
-    for (int i = 0; i < kMax; ++i) {
-        if (i < n) {
-            const int c = i * 32 + lane;
-            const float y = (v[i] - m) * rs * bf16_to_float(w[c]) + bf16_to_float(bias[c]);
-            if (out_bf16) out_bf16[int64_t(r) * D + c] = float_to_bf16(y);
-            if (out_f32) out_f32[int64_t(r) * D + c] = y;
+    for (int k = 0; k < NCK; ++k) {
+        const int c = lane + 32 * k;
+        if (c < nc) {
+            const float gm[8] = {bf16_lo(wv[k].x), bf16_hi(wv[k].x), bf16_lo(wv[k].y), bf16_hi(wv[k].y),
+                                 bf16_lo(wv[k].z), bf16_hi(wv[k].z), bf16_lo(wv[k].w), bf16_hi(wv[k].w)};
+            const float bt[8] = {bf16_lo(bv[k].x), bf16_hi(bv[k].x), bf16_lo(bv[k].y), bf16_hi(bv[k].y),
+                                 bf16_lo(bv[k].z), bf16_hi(bv[k].z), bf16_lo(bv[k].w), bf16_hi(bv[k].w)};
+            float y[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[j] = (v[k][j] - m) * rs * gm[j] + bt[j];
+            if (out_bf16) {
+                uint4 o;
+                o.x = pack_bf16(y[0], y[1]); o.y = pack_bf16(y[2], y[3]);
+                o.z = pack_bf16(y[4], y[5]); o.w = pack_bf16(y[6], y[7]);
+                reinterpret_cast<uint4*>(out_bf16 + int64_t(r) * D)[c] = o;
+            }
+            if (out_f32) {
+                float4* o = reinterpret_cast<float4*>(out_f32 + int64_t(r) * D);
+                o[2 * c] = make_float4(y[0], y[1], y[2], y[3]);
+                o[2 * c + 1] = make_float4(y[4], y[5], y[6], y[7]);
+            }
         }
     }
 }
@@ -594,7 +630,12 @@ cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaS
 cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
                               uint16_t* out_bf16, float* out_f32, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    return launch_pdl(layer_norm_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
+    const dim3 grid((rows + 7) / 8);
+    if (D % 8 != 0 || D > 2048) return cudaErrorInvalidValue;
+    if (D <= 256) return launch_pdl(layer_norm_kernel<1>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
+    if (D <= 512) return launch_pdl(layer_norm_kernel<2>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
+    if (D <= 1024) return launch_pdl(layer_norm_kernel<4>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
+    return launch_pdl(layer_norm_kernel<8>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
 }
 
 cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,
