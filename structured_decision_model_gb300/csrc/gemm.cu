@@ -32,7 +32,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
-constexpr int kMaxSplits = 8;  // cluster size of a split-K tile (portable limit)
+constexpr int kMaxSplits = 4;  // cluster size of a split-K tile (8-CTA clusters did not all fit at once)
 
 struct GemmArgs {
     int n_mtiles, n_ntiles, kblocks;
@@ -341,17 +341,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = threadIdx.x - 64; i < rows * chunks; i += 128) {
                 const int row = id.sp * rows + i / chunks, c = i % chunks;
                 const uint32_t off = red0 + uint32_t((row * kRedLd + c * 16) * 4);
+                // every split's slice is requested before any is added (one round trip),
+                // then the slices are summed in split order
+                float4 w[kMaxSplits][4];
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) {
+                    if (sp < S) {
+                        const uint32_t a = cluster_map(off, uint32_t(sp));
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) w[sp][q] = ld_cluster_f4(a + 16u * q);
+                    }
+                }
                 float v[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = 0.f;
 #pragma unroll
                 for (int sp = 0; sp < kMaxSplits; ++sp) {
                     if (sp < S) {
-                        const uint32_t a = cluster_map(off, uint32_t(sp));
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float4 w = ld_cluster_f4(a + 16u * q);
-                            v[4 * q] += w.x; v[4 * q + 1] += w.y; v[4 * q + 2] += w.z; v[4 * q + 3] += w.w;
+                            v[4 * q] += w[sp][q].x; v[4 * q + 1] += w[sp][q].y;
+                            v[4 * q + 2] += w[sp][q].z; v[4 * q + 3] += w[sp][q].w;
                         }
                     }
                 }
