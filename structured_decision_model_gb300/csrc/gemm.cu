@@ -149,6 +149,47 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int
     }
 }
 
+// The split-K reduction's epilogue (never the LN fold): columns n0 .. n0 + 15 of row m,
+// the bias read from the tile's staged copy `sbias` (column n0 at sbias[0]) and, for
+// EPI_F32_RESID, the residual chunk already loaded into `res`.
+__device__ __forceinline__ void epilogue_chunk_split(const GemmEpilogue& e, int m, int n0, const float* sbias,
+                                                     const float (&acc)[16], const float4 (&res)[4]) {
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = acc[j] + sbias[j];
+    if (e.row_table) {
+        const uint16_t* t = e.row_table + int64_t(e.row_idx[m]) * e.ld_table;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] += bf16_to_float(t[n0 + j]);
+    }
+    if (e.gelu) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = gelu_exact(v[j]);
+    }
+    if (e.kind == EPI_F32 || e.kind == EPI_F32_RESID) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(e.out) + int64_t(m) * e.ldo + n0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float4 w = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            if (e.kind == EPI_F32_RESID) {
+                w.x += res[q].x; w.y += res[q].y; w.z += res[q].z; w.w += res[q].w;
+            }
+            o[q] = w;
+        }
+    } else {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.out) + int64_t(m) * e.ldo + n0);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint4 w;
+            w.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+            w.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+            w.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+            w.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+            o[q] = w;
+        }
+    }
+}
+
 // MC > 1 (B multicast across an M-cluster) is only launched without split-K.
 template <int BN, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -292,6 +333,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; tile_at<MC>(args, it, id); ++it, ++local) {
             const int acc = local & 1;
             const uint32_t use = uint32_t(local >> 1);
+            // split-K: this thread's share of the tile's bias, read while the MMAs run
+            float bias_share[(BN + 127) / 128];
+            if (args.splits > 1) {
+#pragma unroll
+                for (int k = 0; k < (BN + 127) / 128; ++k) {
+                    const int j = (threadIdx.x - 64) + 128 * k, n = id.nt * BN + j;
+                    bias_share[k] = j >= BN ? 0.f
+                                    : args.epi.bias_bf16 ? bf16_to_float(args.epi.bias_bf16[n])
+                                    : (args.epi.bias_f32 ? args.epi.bias_f32[n] : 0.f);
+                }
+            }
             int ok = 1;
             if (lane == 0) ok = mbar_wait_bounded(&tfull[acc], use & 1u, abort_flag, args.dev_flags) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -327,6 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
+            float* sbias = reinterpret_cast<float*>(smem) + BM * kRedLd;  // after the staged rows
+#pragma unroll
+            for (int k = 0; k < (BN + 127) / 128; ++k) {
+                const int j = (threadIdx.x - 64) + 128 * k;
+                if (j < BN) sbias[j] = bias_share[k];
+            }
         }
     }
     if (args.splits > 1) {
@@ -337,10 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int S = args.splits, rows = BM / S;
             constexpr int chunks = BN / 16;
             const uint32_t red0 = smem_u32(smem);
+            const float* sbias = reinterpret_cast<const float*>(smem) + BM * kRedLd;
 #pragma unroll 1
             for (int i = threadIdx.x - 64; i < rows * chunks; i += 128) {
                 const int row = id.sp * rows + i / chunks, c = i % chunks;
                 const uint32_t off = red0 + uint32_t((row * kRedLd + c * 16) * 4);
+                const int m = id.mt * BM + row;
+                const int n0 = id.nt * BN + c * 16;
+                float4 res[4];
+                if (args.epi.kind == EPI_F32_RESID && m < args.epi.M) {  // read ahead of the partial sums
+                    const float4* o = reinterpret_cast<const float4*>(static_cast<const float*>(args.epi.out) +
+                                                                      int64_t(m) * args.epi.ldo + n0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) res[q] = o[q];
+                }
                 // every split's slice is requested before any is added (one round trip),
                 // then the slices are summed in split order
                 float4 w[kMaxSplits][4];
@@ -365,13 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                const int m = id.mt * BM + row;
-                if (m < args.epi.M) {
-                    uint32_t r[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(v[j]);
-                    epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r);
-                }
+                if (m < args.epi.M) epilogue_chunk_split(args.epi, m, n0, sbias + c * 16, v, res);
             }
         }
         cluster_sync();  // no CTA leaves while another may still read its shared memory
