@@ -339,9 +339,15 @@ __global__ void __launch_bounds__(256) field_pool_kernel(const float* __restrict
     const int j0 = q_opt_off[q], n = q_opt_off[q + 1] - j0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int j = warp; j < n; j += 8) {
-        const float* row = o_hat + int64_t(j0 + j) * D;
+        const float4* row = reinterpret_cast<const float4*>(o_hat + int64_t(j0 + j) * D);
+        const uint2* w2 = reinterpret_cast<const uint2*>(w_a);
         float s = 0.f;
-        for (int c = lane; c < D; c += 32) s += row[c] * bf16_to_float(w_a[c]);
+#pragma unroll 8
+        for (int c = lane; c < D / 4; c += 32) {
+            const float4 x = row[c];
+            const uint2 w = w2[c];
+            s += x.x * bf16_lo(w.x) + x.y * bf16_hi(w.x) + x.z * bf16_lo(w.y) + x.w * bf16_hi(w.y);
+        }
         s = warp_sum(s);
         if (lane == 0) sc[j] = s + bf16_to_float(b_a[0]);
     }
@@ -357,10 +363,16 @@ __global__ void __launch_bounds__(256) field_pool_kernel(const float* __restrict
         for (int j = lane; j < n; j += 32) sc[j] = expf(sc[j] - m) / z;
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        float s = 0.f;
-        for (int j = 0; j < n; ++j) s += sc[j] * o_hat[int64_t(j0 + j) * D + c];
-        out[int64_t(q) * ldo + col_off + c] = float_to_bf16(s);
+    for (int c = threadIdx.x; c < D / 4; c += blockDim.x) {  // 4 columns per thread
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const float a = sc[j];
+            const float4 x = reinterpret_cast<const float4*>(o_hat + int64_t(j0 + j) * D)[c];
+            acc.x += a * x.x; acc.y += a * x.y; acc.z += a * x.z; acc.w += a * x.w;
+        }
+        *reinterpret_cast<uint2*>(out + int64_t(q) * ldo + col_off + 4 * c) =
+            make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
     }
 }
 
@@ -379,12 +391,20 @@ __global__ void __launch_bounds__(128) field_attn_kernel(const uint16_t* __restr
     __shared__ float sp[kMaxFields][kMaxFields + 1];
     const int b = blockIdx.x, h = blockIdx.y;
     const int q0 = rec_q_off[b], n = rec_q_off[b + 1] - q0;
-    for (int i = threadIdx.x; i < n * 64; i += blockDim.x) {
-        const int r = i >> 6, c = i & 63;
-        const uint16_t* row = qkv + int64_t(q0 + r) * 3 * D + h * 64 + c;
-        sq[r][c] = bf16_to_float(row[0]);
-        sk[r][c] = bf16_to_float(row[D]);
-        sv[r][c] = bf16_to_float(row[2 * D]);
+    // 16-byte loads: thread i takes columns 8 (i % 8) .. + 7 of field i / 8 of q, k and v
+    for (int i = threadIdx.x; i < n * 8; i += blockDim.x) {
+        const int r = i >> 3, c8 = (i & 7) * 8;
+        const uint16_t* row = qkv + int64_t(q0 + r) * 3 * D + h * 64 + c8;
+        const uint4 a = *reinterpret_cast<const uint4*>(row);
+        const uint4 bk = *reinterpret_cast<const uint4*>(row + D);
+        const uint4 bv = *reinterpret_cast<const uint4*>(row + 2 * D);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wk[4] = {bk.x, bk.y, bk.z, bk.w}, wv[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            sq[r][c8 + 2 * j] = bf16_lo(wa[j]); sq[r][c8 + 2 * j + 1] = bf16_hi(wa[j]);
+            sk[r][c8 + 2 * j] = bf16_lo(wk[j]); sk[r][c8 + 2 * j + 1] = bf16_hi(wk[j]);
+            sv[r][c8 + 2 * j] = bf16_lo(wv[j]); sv[r][c8 + 2 * j + 1] = bf16_hi(wv[j]);
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < n * n; i += blockDim.x) {
@@ -405,11 +425,19 @@ __global__ void __launch_bounds__(128) field_attn_kernel(const uint16_t* __restr
         for (int c = 0; c < n; ++c) sp[r][c] *= inv;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < n * 64; i += blockDim.x) {
-        const int r = i >> 6, d = i & 63;
-        float s = 0.f;
-        for (int c = 0; c < n; ++c) s += sp[r][c] * sv[c][d];
-        out[int64_t(q0 + r) * D + h * 64 + d] = float_to_bf16(s);
+    // thread i writes columns 8 (i % 8) .. + 7 of field i / 8 with one 16-byte store
+    for (int i = threadIdx.x; i < n * 8; i += blockDim.x) {
+        const int r = i >> 3, c8 = (i & 7) * 8;
+        float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < n; ++c) {
+            const float p = sp[r][c];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] += p * sv[c][c8 + j];
+        }
+        uint4 w;
+        w.x = pack_bf16(o[0], o[1]); w.y = pack_bf16(o[2], o[3]);
+        w.z = pack_bf16(o[4], o[5]); w.w = pack_bf16(o[6], o[7]);
+        *reinterpret_cast<uint4*>(out + int64_t(q0 + r) * D + h * 64 + c8) = w;
     }
 }
 
