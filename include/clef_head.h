@@ -219,6 +219,17 @@ CLEF_API int clef_stream_finish(const clef_config* cfg, const void* const* weigh
  * the status covers the latest call on the workspace. */
 CLEF_API int clef_device_status(void* workspace, void* stream);
 
+/* Self-test of the device-side wait limits (the pages have no counterpart: this is a
+ * property of this implementation).  Clears the status word of `workspace` (device
+ * memory, 256-byte aligned, at least 256 bytes) and launches one kernel whose single
+ * waiting thread waits on a barrier that never completes, for `limit_ns` nanoseconds
+ * (1 us .. 100 ms).  The wait gives up, sets the timeout bit and the kernel returns:
+ * clef_device_status then reports CLEF_ERR_DEVICE_TIMEOUT and the CUDA context stays
+ * usable.  Every wait of the head's own kernels has the same form, with a 2 s limit.
+ * Returns CLEF_ERR_INVALID_ARGUMENT for a null or misaligned workspace or a limit out
+ * of range, CLEF_ERR_CUDA if the launch fails, else CLEF_OK (asynchronously). */
+CLEF_API int clef_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* stream);
+
 /* Index check of the pooling step ("clef-4bit JointSchemaHead walkthrough" section 3
  * step 1): un-normalised fp32 sums of the raw hidden rows over every instruction span
  * (q_sum [Q][H]) and option span (o_sum [O][H]) and of the lexical rows under every

@@ -21,7 +21,7 @@ EXPORTED = [
     "clef_weight_count", "clef_prepared_size", "clef_prepare_weights", "clef_workspace_size",
     "clef_head_forward", "clef_device_status", "clef_span_sums", "clef_gemm_bf16",
     "clef_kernel_launches", "clef_status_string", "clef_span_sums_noalloc", "clef_stream_begin",
-    "clef_stream_rows", "clef_stream_finish",
+    "clef_stream_rows", "clef_stream_finish", "clef_selftest_wait_timeout",
 ]
 
 _i32, _i64, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
@@ -70,6 +70,7 @@ def load():
                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                       ctypes.POINTER(ClefDebugOutputs), _vp]
     lib.clef_device_status.argtypes = [_vp, _vp]
+    lib.clef_selftest_wait_timeout.argtypes = [_vp, _i64, _vp]
     lib.clef_stream_begin.argtypes = [ctypes.POINTER(ClefConfig), ctypes.POINTER(ClefSchema), _vp, _sz, _vp]
     lib.clef_stream_rows.argtypes = [ctypes.POINTER(ClefConfig), _vp, ctypes.POINTER(ClefSchema), _vp, _i32, _i32,
                                      _i32, _vp, _sz, _vp]
@@ -186,6 +187,13 @@ def clef_kernel_launches():
 
 def clef_device_status(workspace_ptr, stream=0):
     return load().clef_device_status(workspace_ptr, stream)
+
+
+def clef_selftest_wait_timeout(workspace_ptr, limit_ns, stream=0, check=True):
+    st = load().clef_selftest_wait_timeout(workspace_ptr, int(limit_ns), stream)
+    if check:
+        _check(st, "clef_selftest_wait_timeout")
+    return st
 
 
 def clef_span_sums(cfg, schema: Schema, hidden_ptr, token_ids_ptr, lexical_ptr, q_sum_ptr, o_sum_ptr, x_sum_ptr,

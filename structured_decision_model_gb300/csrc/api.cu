@@ -686,6 +686,15 @@ int clef_device_status(void* workspace, void* stream) {
     return CLEF_OK;
 }
 
+int clef_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) || limit_ns < 1000 || limit_ns > 100000000)
+        return CLEF_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CK(cudaMemsetAsync(workspace, 0, 256, st));
+    CK(launch_wait_timeout_selftest(static_cast<int*>(workspace), uint64_t(limit_ns), st));
+    return CLEF_OK;
+}
+
 int clef_span_sums(const clef_config* cfg, const clef_schema* schema, const uint16_t* hidden,
                    const int32_t* token_ids, const uint16_t* lexical, float* q_sum, float* o_sum, float* x_sum,
                    void* workspace, size_t workspace_bytes, void* stream) {

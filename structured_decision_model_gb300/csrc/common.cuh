@@ -112,7 +112,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // out, or returns false at once when another role of the CTA has already aborted
 // (abort_flag may be null for a wait that must not be cut short by an abort).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                  int* dev_flags) {
+                                                  int* dev_flags, uint64_t limit_ns = kWaitLimitNs) {
     uint64_t start = 0;
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -120,7 +120,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             if (abort_flag && *abort_flag) return false;
             const uint64_t now = global_ns();
             if (start == 0) start = now;
-            else if (now - start > kWaitLimitNs) break;
+            else if (now - start > limit_ns) break;
         }
     }
     if (abort_flag) *abort_flag = 1;

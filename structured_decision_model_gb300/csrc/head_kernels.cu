@@ -627,7 +627,27 @@ __global__ void __launch_bounds__(256) copy_cols_kernel(uint16_t* __restrict__ d
         *reinterpret_cast<const uint4*>(src + int64_t(r) * ld_src + c);
 }
 
+// =====================================================================
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing ever
+// completes, with a short limit, so the wait runs out, sets the timeout bit of the
+// status word and returns.  No thread hangs and nothing faults.
+// =====================================================================
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(int* flags, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        mbar_wait_bounded(&bar, 0, nullptr, flags, limit_ns);  // phase 0 never completes
+    }
+    __syncwarp();
+}
+
 // ----------------------------------------------------------------- launchers
+
+cudaError_t launch_wait_timeout_selftest(int* flags, uint64_t limit_ns, cudaStream_t s) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(flags, limit_ns);
+    return counted(cudaGetLastError());
+}
 
 cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpad, int H, const int32_t* tile_rec,
                              const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,

@@ -72,6 +72,7 @@ cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpa
                              cudaStream_t s);
 cudaError_t launch_row_stats_rows(const uint16_t* rows, int64_t row_stride, int H, int n, float* mu, float* rstd,
                                   cudaStream_t s);
+cudaError_t launch_wait_timeout_selftest(int* flags, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off, const int32_t* lengths, int B,
                               cudaStream_t s);
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s);

@@ -193,3 +193,11 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
         B.load()
     with pytest.raises(FileNotFoundError):
         B.clef_weight_count(B.make_config())
+
+
+def test_selftest_wait_timeout_validation():
+    """Bad workspace pointers or limits are rejected before anything is launched."""
+    assert B.clef_selftest_wait_timeout(0, 1_000_000, check=False) == 1
+    assert B.clef_selftest_wait_timeout((1 << 20) + 16, 1_000_000, check=False) == 1
+    assert B.clef_selftest_wait_timeout(1 << 20, 10, check=False) == 1
+    assert B.clef_selftest_wait_timeout(1 << 20, 10**9, check=False) == 1
