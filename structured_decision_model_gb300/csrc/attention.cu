@@ -166,8 +166,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             qs = 0;
             qphase ^= 1u;
         }
-        float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+        float m_r[2] = {-INFINITY, -INFINITY};
         float acc[8][4];
+        // running sums of P per row, from an extra MMA of P against an all-ones block:
+        // lsum[0..1] row g, lsum[2..3] row g + 8 (the n columns are equal)
+        float lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 // The row's reference maximum m moves only when a tile's maximum exceeds it by
                 // more than 2^8 (p never exceeds 2^8, so nothing overflows); the accumulator and
                 // the running sum are rescaled only then, which after the first tile is rare.
-                float ps[2] = {0.f, 0.f}, nm[2];
+                float nm[2];
                 bool need[2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
@@ -225,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                         const float mn = need[r] ? mx[r] : m_r[r];
                         const float corr = ex2_approx(m_r[r] - mn);
                         m_r[r] = mn;
-                        l_r[r] *= corr;
+                        lsum[2 * r] *= corr;
+                        lsum[2 * r + 1] *= corr;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             acc[j][2 * r] *= corr;
@@ -240,13 +244,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 for (int j = 0; j < 8; ++j) {
                     const float p0 = ex2_approx(fmaf(s[j][0], sl2, nm[0])), p1 = ex2_approx(fmaf(s[j][1], sl2, nm[0]));
                     const float p2 = ex2_approx(fmaf(s[j][2], sl2, nm[1])), p3 = ex2_approx(fmaf(s[j][3], sl2, nm[1]));
-                    ps[0] += p0 + p1;
-                    ps[1] += p2 + p3;
                     pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
                     pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
                 }
-#pragma unroll
-                for (int r = 0; r < 2; ++r) l_r[r] += ps[r];
+                constexpr uint32_t kOnes = 0x3F803F80u;  // two bf16 1.0
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                         mma_bf16_16816(acc[2 * dp], pa[ks], vr[0], vr[1]);
                         mma_bf16_16816(acc[2 * dp + 1], pa[ks], vr[2], vr[3]);
                     }
+                    mma_bf16_16816(lsum, pa[ks], kOnes, kOnes);  // the rows of P summed
                 }
             }
             __syncwarp();
@@ -266,11 +268,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
         }
         if (!active) continue;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-        }
+        const float l_r[2] = {lsum[0], lsum[2]};
         const int64_t part_base = a.rec_part_off[k.b] + (int64_t(k.kc) * a.heads + k.h) * k.O_b;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
