@@ -204,11 +204,14 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 }
                 // raw-score row maxima; the scale is applied once per row and fused into the
                 // exponent below (p = 2^(s * scale - m))
-                float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
-                    mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
+                float mx[2];
+                #pragma unroll
+                for (int r = 0; r < 2; ++r) {  // 16 values of row g (r = 0) or g + 8 (r = 1): a 3-input max tree
+                    const int c0 = 2 * r;
+                    const float a = fmax3(s[0][c0], s[0][c0 + 1], s[1][c0]), b = fmax3(s[1][c0 + 1], s[2][c0], s[2][c0 + 1]);
+                    const float c = fmax3(s[3][c0], s[3][c0 + 1], s[4][c0]), d = fmax3(s[4][c0 + 1], s[5][c0], s[5][c0 + 1]);
+                    const float e = fmax3(s[6][c0], s[6][c0 + 1], s[7][c0]);
+                    mx[r] = fmaxf(fmax3(a, b, c), fmax3(d, e, s[7][c0 + 1]));
                 }
                 // The row's reference maximum m moves only when a tile's maximum exceeds it by
                 // more than 2^8 (p never exceeds 2^8, so nothing overflows); the accumulator and
