@@ -299,6 +299,7 @@ cudaError_t dense(const uint16_t* A, int64_t lda, int M, const uint16_t* Bw, int
                   int* flags, cudaStream_t st) {
     GemmProblem g;
     g.allow_split = true;
+    g.b_is_weight = true;
     g.A = A;
     g.lda = lda;
     g.a_rows = M;

@@ -42,6 +42,7 @@ struct GemmArgs {
     const int32_t* a_row_of_mtile;
     GemmEpilogue epi;
     int* dev_flags;
+    int prefetch_b;                // B tiles of the first stages may be requested before the PDL wait
 };
 
 // Tile t of the persistent walk: split fastest, then N, then M.
@@ -238,10 +239,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (MC > 1) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int kblocks = args.kblocks;
+    // When B holds weights, the producer requests the B tiles of the first stages of its
+    // first tile before the dependent-launch wait: only A (and the epilogue's inputs) may
+    // come from the previous kernel.  Each such stage is armed for its full A + B byte
+    // count now; its A tile follows once the wait returns.
+    int n_pre = 0;
+    if constexpr (MC == 1) {
+        TileId id0;
+        if (args.prefetch_b && warp == 0 && lane == 0 && tile_at<MC>(args, 0, id0)) {
+            const int kb0 = id0.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
+            n_pre = min(C::STAGES, kb1 - kb0);
+            for (int i = 0; i < n_pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], C::A_BYTES + C::B_BYTES);
+                tma_load_2d(sB + i * C::B_BYTES, &tmB, (kb0 + i) * BK, id0.nt * BN, &full[i]);
+            }
+        }
+    }
     griddep_launch();
     griddep_wait();  // operands and outputs may belong to the previous kernel of the stream
-
-    const int kblocks = args.kblocks;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -257,18 +273,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b_row = id.nt * BN;
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.dev_flags)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
-                    tma_load_2d(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, &full[stage]);
-                    if constexpr (MC == 1) {
-                        tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
+                    const bool pre = n_pre > 0;  // stage armed and its B requested before the wait
+                    if (pre) {
+                        --n_pre;
                     } else {
-                        const int r = int(blockIdx.x) % MC;
-                        tma_load_2d_mc(sB + stage * C::B_BYTES + r * (C::B_BYTES / MC), &tmBp, kb * BK,
-                                       b_row + r * (BN / MC), &full[stage], kPeers);
+                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.dev_flags)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
+                    }
+                    tma_load_2d(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, &full[stage]);
+                    if (!pre) {
+                        if constexpr (MC == 1) {
+                            tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
+                        } else {
+                            const int r = int(blockIdx.x) % MC;
+                            tma_load_2d_mc(sB + stage * C::B_BYTES + r * (C::B_BYTES / MC), &tmBp, kb * BK,
+                                           b_row + r * (BN / MC), &full[stage], kPeers);
+                        }
                     }
                     ++armed[stage];
                     if (++stage == C::STAGES) {
@@ -595,6 +618,7 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     a.a_row_of_mtile = p.a_row_of_mtile;
     a.epi = e;
     a.dev_flags = flags;
+    a.prefetch_b = p.b_is_weight ? 1 : 0;
     const int sms = num_sms();
     const int out_tiles = a.n_mtiles * a.n_ntiles;
     const int tiles = out_tiles * a.splits;

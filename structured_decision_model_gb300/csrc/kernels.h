@@ -73,6 +73,9 @@ struct GemmProblem {
     // split K across a thread-block cluster when the output tiles cannot fill the GPU
     // (needs no scratch: the partial tiles are summed in distributed shared memory)
     bool allow_split = false;
+    // B is never written by a kernel that may still be running on the stream (weights): its
+    // first tiles may then be requested before waiting for the previous kernel of the stream
+    bool b_is_weight = false;
 };
 
 int num_sms();
