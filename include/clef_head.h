@@ -253,10 +253,11 @@ CLEF_API int clef_span_sums(const clef_config* cfg, const clef_schema* schema, c
  *     one static device array of CLEF_SPAN_SUMS_NOALLOC_SCRATCH_BYTES (1 MiB) inside
  *     the library.  Every GPU that loads the library holds that array until the
  *     process exits.  A schema whose plan does not fit returns
- *     CLEF_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The plan takes 28
- *     bytes per question, 24 per option, 32 per record and 8 per 128 memory rows, so
- *     1 MiB holds, for example, 2 000 questions and 20 000 options over 256 records
- *     of 16 384 rows.
+ *     CLEF_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The plan takes 36
+ *     bytes per question, 32 per option, 40 per record, 8 per 128 memory rows and 16
+ *     per 1024 memory rows (more for records with over 64 options), so 1 MiB holds,
+ *     for example, 1 500 questions and 15 000 options over 256 records of 16 384
+ *     rows.
  *   - The caller passes inputs and outputs exactly as for clef_span_sums, and gets
  *     the same sums bit for bit.
  *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.

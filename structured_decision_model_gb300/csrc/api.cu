@@ -69,7 +69,7 @@ struct Plan {
     std::vector<int32_t> blob;  // int32 tables followed by the int64 partial offsets
     // offsets (in int32 units) of each table in the blob
     size_t lengths, rec_row_off, rec_q_off, rec_o_off, q_rec, q_type, q_span, q_opt_off, o_rec, o_q, o_span,
-        tile_rec, tile_a_row, item_kind, item_index, chunk_rec, chunk_idx, unit_cx, unit_qp, rec_part_off;
+        tile_rec, tile_a_row, item, chunk_rec, chunk_idx, unit_cx, unit_qp, rec_part_off;
 };
 
 int validate_schema(const clef_config* c, const clef_schema* s) {
@@ -178,8 +178,8 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
         }
     }
     p.n_items = Q + O + B;
-    p.item_kind = put(p.n_items);
-    p.item_index = put(p.n_items);
+    while (v.size() % 4) v.push_back(0);  // the item table's rows are 16-byte aligned
+    p.item = put(4 * size_t(p.n_items));
     {
         // pooling work items, most rows first (option items read two rows per span row),
         // so that the last wave of CTAs holds the short ones
@@ -192,9 +192,26 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
                          [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
         for (int i = 0; i < p.n_items; ++i) {
             const int id = cost[i].second;
-            const int kind = id < Q ? 0 : (id < Q + O ? 1 : 2);
-            v[p.item_kind + i] = kind;
-            v[p.item_index + i] = kind == 0 ? id : (kind == 1 ? id - Q : id - Q - O);
+            // one row per item: {kind << 30 | index, record, span start, span end}
+            int32_t* row = &v[p.item + 4 * size_t(i)];
+            if (id < Q) {
+                row[0] = id;
+                row[1] = s->q_rec[id];
+                row[2] = s->q_span[2 * id];
+                row[3] = s->q_span[2 * id + 1];
+            } else if (id < Q + O) {
+                const int j = id - Q;
+                row[0] = (1 << 30) | j;
+                row[1] = v[p.o_rec + j];
+                row[2] = s->o_span[2 * j];
+                row[3] = s->o_span[2 * j + 1];
+            } else {
+                const int b = id - Q - O;
+                row[0] = (2 << 30) | b;
+                row[1] = b;
+                row[2] = s->lengths[b] - 1;
+                row[3] = s->lengths[b];
+            }
         }
     }
     p.n_chunks = nch;
@@ -475,7 +492,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     sp.hidden = hidden; sp.row_stride = schema->row_stride; sp.Lpad = schema->Lpad; sp.H = H; sp.vocab = cfg->vocab;
     sp.token_ids = token_ids; sp.lexical = lexical; sp.mu = mu; sp.rstd = rstd;
     sp.ln_w = W(weights, 0); sp.ln_b = W(weights, 1);
-    sp.item_kind = T(p.item_kind); sp.item_index = T(p.item_index);
+    sp.items = reinterpret_cast<const int4*>(T(p.item));
     sp.lengths = T(p.lengths); sp.rec_row_off = T(p.rec_row_off); sp.rec_q_off = T(p.rec_q_off);
     sp.q_rec = T(p.q_rec); sp.q_span = T(p.q_span); sp.q_opt_off = T(p.q_opt_off);
     sp.o_rec = T(p.o_rec); sp.o_span = T(p.o_span);
@@ -719,7 +736,7 @@ int clef_span_sums(const clef_config* cfg, const clef_schema* schema, const uint
     SpanPoolArgs sp{};
     sp.hidden = hidden; sp.row_stride = schema->row_stride; sp.Lpad = schema->Lpad; sp.H = cfg->hidden;
     sp.vocab = cfg->vocab; sp.token_ids = token_ids; sp.lexical = lexical;
-    sp.item_kind = plan + p.item_kind; sp.item_index = plan + p.item_index;
+    sp.items = reinterpret_cast<const int4*>(plan + p.item);
     sp.lengths = plan + p.lengths; sp.rec_row_off = plan + p.rec_row_off; sp.rec_q_off = plan + p.rec_q_off;
     sp.q_rec = plan + p.q_rec; sp.q_span = plan + p.q_span; sp.q_opt_off = plan + p.q_opt_off;
     sp.o_rec = plan + p.o_rec; sp.o_span = plan + p.o_span;
@@ -809,7 +826,7 @@ int clef_span_sums_noalloc(const clef_config* cfg, const clef_schema* schema, co
     SpanPoolArgs sp{};
     sp.hidden = hidden; sp.row_stride = schema->row_stride; sp.Lpad = schema->Lpad; sp.H = cfg->hidden;
     sp.vocab = cfg->vocab; sp.token_ids = token_ids; sp.lexical = lexical;
-    sp.item_kind = plan + p.item_kind; sp.item_index = plan + p.item_index;
+    sp.items = reinterpret_cast<const int4*>(plan + p.item);
     sp.lengths = plan + p.lengths; sp.rec_row_off = plan + p.rec_row_off; sp.rec_q_off = plan + p.rec_q_off;
     sp.q_rec = plan + p.q_rec; sp.q_span = plan + p.q_span; sp.q_opt_off = plan + p.q_opt_off;
     sp.o_rec = plan + p.o_rec; sp.o_span = plan + p.o_span;

@@ -114,18 +114,13 @@ template <bool RAW>
 __global__ void __launch_bounds__(256, 3) span_pool_kernel(SpanPoolArgs a) {
     griddep_wait();
     griddep_launch();
-    const int kind = a.item_kind[blockIdx.x];
-    const int idx = a.item_index[blockIdx.x];
+    // the item, its record and its span in one 16-byte load (no dependent table lookups)
+    const int4 it = a.items[blockIdx.x];
+    const int kind = int(uint32_t(it.x) >> 30);
+    const int idx = it.x & ((1 << 30) - 1);
     const int H = a.H;
     const int n8 = H >> 3;
-    int b, s, e;
-    if (kind == 0) {
-        b = a.q_rec[idx]; s = a.q_span[2 * idx]; e = a.q_span[2 * idx + 1];
-    } else if (kind == 1) {
-        b = a.o_rec[idx]; s = a.o_span[2 * idx]; e = a.o_span[2 * idx + 1];
-    } else {
-        b = idx; s = a.lengths[b] - 1; e = s + 1;
-    }
+    const int b = it.y, s = it.z, e = it.w;
     const int64_t rec_base = int64_t(b) * a.Lpad;
     const int stat_base = a.rec_row_off[b];
     const float inv_n = 1.0f / float(e - s);

@@ -17,7 +17,7 @@ struct SpanPoolArgs {
     const int32_t* token_ids; const uint16_t* lexical;
     const float* mu; const float* rstd;          // compact-row statistics
     const uint16_t* ln_w; const uint16_t* ln_b;  // memory LayerNorm affine
-    const int32_t* item_kind; const int32_t* item_index;
+    const int4* items;                           // per item {kind << 30 | index, record, span start, span end}
     const int32_t* lengths; const int32_t* rec_row_off; const int32_t* rec_q_off;
     const int32_t* q_rec; const int32_t* q_span; const int32_t* q_opt_off;
     const int32_t* o_rec; const int32_t* o_span;
