@@ -599,15 +599,21 @@ __global__ void __launch_bounds__(256) fold_kv_kernel(FoldArgs a) {
 
 // Launch-plan upload: the host's plan tables travel as kernel parameters (copied by
 // the launch itself, so no host buffer has to outlive the call and nothing waits).
-struct PlanChunk {
+struct alignas(16) PlanChunk {
+    int32_t data[kPlanChunkInts];  // first: 16-byte aligned for vector reads
     int32_t n;
-    int32_t data[kPlanChunkInts];
 };
+static_assert(kPlanChunkInts % 4 == 0, "plan chunks start on 16-byte boundaries of the destination");
 
-__global__ void __launch_bounds__(256) plan_upload_kernel(int32_t* __restrict__ dst, const PlanChunk c) {
+// One 16-byte unit per thread over several CTAs (reads of the parameter block by
+// different lanes do not broadcast, so the copy is spread out); dst is 16-byte aligned.
+__global__ void __launch_bounds__(256) plan_upload_kernel(int32_t* __restrict__ dst, const __grid_constant__ PlanChunk c) {
     griddep_wait();
     griddep_launch();
-    for (int i = threadIdx.x; i < c.n; i += blockDim.x) dst[i] = c.data[i];
+    const int i = int(blockIdx.x * blockDim.x + threadIdx.x);
+    const int n4 = c.n >> 2;
+    if (i < n4) reinterpret_cast<int4*>(dst)[i] = reinterpret_cast<const int4*>(c.data)[i];
+    if (i < (c.n & 3)) dst[4 * n4 + i] = c.data[4 * n4 + i];
 }
 
 // dst[r][col_off + c] = src[r][c] for a [rows][cols] bf16 block (16-byte units).
@@ -711,7 +717,8 @@ cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaS
     for (size_t off = 0; off < n; off += kPlanChunkInts) {
         c.n = int32_t(n - off < size_t(kPlanChunkInts) ? n - off : size_t(kPlanChunkInts));
         for (int i = 0; i < c.n; ++i) c.data[i] = src[off + i];
-        const cudaError_t e = launch_pdl(plan_upload_kernel, dim3(1), dim3(256), 0, s, dst + off, c);
+        const unsigned grid = unsigned((c.n + 1023) / 1024);
+        const cudaError_t e = launch_pdl(plan_upload_kernel, dim3(grid), dim3(256), 0, s, dst + off, c);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
