@@ -604,6 +604,7 @@ struct alignas(16) PlanChunk {
     int32_t n;
 };
 static_assert(kPlanChunkInts % 4 == 0, "plan chunks start on 16-byte boundaries of the destination");
+static_assert(sizeof(PlanChunk) + sizeof(int32_t*) <= 32764, "kernel parameters are limited to 32,764 bytes");
 
 // One 16-byte unit per thread over several CTAs (reads of the parameter block by
 // different lanes do not broadcast, so the copy is spread out); dst is 16-byte aligned.

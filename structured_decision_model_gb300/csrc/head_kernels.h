@@ -10,7 +10,7 @@ constexpr int kAttnChunk = 1024;  // memory rows per split-L routing-attention w
 constexpr int kAttnQRows = 64;    // option queries per routing-attention work item
 constexpr int kMaxFields = 48;    // questions per record handled by the field self-attention kernel
 constexpr int kMaxOptions = 256;  // options per question
-constexpr int kPlanChunkInts = 4000;  // plan ints carried by one upload launch (16 KB of parameters)
+constexpr int kPlanChunkInts = 8000;  // plan ints carried by one upload launch (32 KB of parameters)
 
 struct SpanPoolArgs {
     const uint16_t* hidden; int64_t row_stride; int Lpad; int H; int vocab;
