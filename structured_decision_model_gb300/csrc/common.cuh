@@ -108,14 +108,35 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Arrive (release at cluster scope) on an mbarrier of another CTA of the cluster;
+// `bar` is a cluster address from cluster_map.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// mbar_try_wait with acquire at cluster scope: for barriers that other CTAs of the
+// cluster arrive on, so that what they wrote before arriving is visible after.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: returns false (and sets the timeout flag) when the time limit runs
 // out, or returns false at once when another role of the CTA has already aborted
 // (abort_flag may be null for a wait that must not be cut short by an abort).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                  int* dev_flags, uint64_t limit_ns = kWaitLimitNs) {
+                                                  int* dev_flags, uint64_t limit_ns = kWaitLimitNs,
+                                                  bool cluster_scope = false) {
     uint64_t start = 0;
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 255u) {
             if (abort_flag && *abort_flag) return false;
             const uint64_t now = global_ns();
@@ -139,15 +160,14 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
-// The same load, multicast: the tile lands at the same shared-memory offset in every
-// CTA of the cluster named in `mask`, and each of those CTAs' mbarrier at `bar`'s
-// offset receives the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                               uint64_t* bar, uint16_t mask) {
+// Load by one CTA of a pair into its own shared memory, completing the bytes on an
+// mbarrier of either CTA of the pair (`bar`: a cluster address from cluster_map).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
 
@@ -194,13 +214,42 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// The same, arriving on the mbarrier at `bar`'s offset in every CTA of the cluster in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+// ------------------------------------------------ tcgen05, CTA pairs (cta_group::2)
+// A kernel uses either the single-CTA forms above or these: every tcgen05
+// allocation, MMA and commit of one kernel names the same CTA group.  In a pair
+// (the two CTAs of a 2-CTA cluster, ranks 0 and 1) one MMA computes a 256-row tile:
+// rows 0..127 come from rank 0's shared memory and land in rank 0's TMEM, rows
+// 128..255 from rank 1's; the B tile is split along N the same way, and both halves
+// sit at the same shared-memory offset in the two CTAs.
+
+// One warp of EACH CTA of the pair executes this; both receive the same address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Issued by one thread of rank 0: D(tmem, both CTAs) (+)= A(both CTAs) * B(both CTAs)^T.
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Arrive on the mbarrier at cluster address `bar` (this CTA's or the peer's, from
+// cluster_map) once every pair MMA issued so far by this thread completes.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns: thread i of the warp gets lane (base + i).

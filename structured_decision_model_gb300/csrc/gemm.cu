@@ -11,6 +11,8 @@
 // accumulators let the epilogue of one tile overlap the mainloop of the next.
 // Operand tiles are 64-element K slices with the 128-byte swizzle.  Tiles are
 // visited N-fastest so that CTAs working at the same time share A tiles in L2.
+// Operand-heavy launches of 256-wide tiles run as CTA pairs (cta_group::2): two SMs
+// compute one 256 x 256 tile, each loading half of its operands.
 // Small-M projections whose tiles cannot fill the GPU split K: the S parts of one
 // output tile run as one thread-block cluster, each stages its fp32 accumulator in
 // its own shared memory, and after a cluster barrier CTA rank r sums rows
@@ -58,33 +60,35 @@ __device__ __forceinline__ TileId decode_tile(const GemmArgs& a, int t) {
     return id;
 }
 
-// The it-th tile of this CTA's persistent walk.  MC == 1: tiles t = blockIdx.x + it *
-// gridDim.x.  MC > 1: the CTAs of a cluster take MC consecutive M tiles of one N tile
-// (rank r takes M tile MC * group + r) and walk the groups together, so that each can
-// multicast its 1/MC share of the common B tile to all of them.
-template <int MC>
+// The it-th tile of this CTA's persistent walk.  Single CTAs: tiles t = blockIdx.x +
+// it * gridDim.x.  CTA pairs: the two CTAs of a cluster take two consecutive M tiles
+// of one N tile (rank r takes M tile 2 * group + r: the pair's 256-row tile) and walk
+// the groups together.
+template <bool PAIR>
 __device__ __forceinline__ bool tile_at(const GemmArgs& a, int it, TileId& id) {
-    if constexpr (MC == 1) {
+    if constexpr (!PAIR) {
         const int t = int(blockIdx.x) + it * int(gridDim.x);
         if (t >= a.n_mtiles * a.n_ntiles * a.splits) return false;
         id = decode_tile(a, t);
         return true;
     } else {
-        const int g = int(blockIdx.x) / MC + it * (int(gridDim.x) / MC);
-        if (g >= (a.n_mtiles + MC - 1) / MC * a.n_ntiles) return false;
+        const int g = int(blockIdx.x) / 2 + it * (int(gridDim.x) / 2);
+        if (g >= (a.n_mtiles + 1) / 2 * a.n_ntiles) return false;
         id.sp = 0;
         id.nt = g % a.n_ntiles;
-        id.mt = (g / a.n_ntiles) * MC + int(blockIdx.x) % MC;
+        id.mt = (g / a.n_ntiles) * 2 + int(blockIdx.x) % 2;
         id.out = id.mt * a.n_ntiles + id.nt;
         return true;
     }
 }
 
-template <int BN>
+// PAIR: each CTA holds its 128 A rows and half (BN / 2 rows) of the pair's B tile.
+template <int BN, bool PAIR>
 struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
     static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
@@ -191,13 +195,22 @@ __device__ __forceinline__ void epilogue_chunk_split(const GemmEpilogue& e, int 
     }
 }
 
-// MC > 1 (B multicast across an M-cluster) is only launched without split-K.
-template <int BN, int MC>
+// PAIR (CTA pairs on cta_group::2) is only launched without split-K.
+//
+// CTA pairs.  Each CTA's producer loads its own A tile (128 rows) and its half of the
+// pair's B tile into its own shared memory.  Rank 0 issues the pair's MMAs (M = 256),
+// so every copy of both CTAs completes its bytes on rank 0's `full` barrier (rank 1
+// names it through the cta_group::2 form of the copy), which rank 0's producer arms
+// for both CTAs' bytes.  Rank 0's MMA thread commits every stage to the `empty`
+// barriers of both CTAs and every finished accumulator to the `tfull` barriers of
+// both; the epilogue warps of both CTAs arrive on rank 0's `tempty`.  Rank 1 cannot
+// observe its own copies land (they complete on rank 0), so it leaves only through
+// the final cluster barrier, after rank 0 has consumed or waited for every stage.
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmBp, const GemmArgs args) {
-    using C = GemmCfg<BN>;
-    constexpr uint16_t kPeers = uint16_t((1u << MC) - 1u);  // multicast mask: every CTA of the cluster
+                   const GemmArgs args) {
+    using C = GemmCfg<BN, PAIR>;
     constexpr int kRedLd = BN + 4;  // staged split-K row stride (floats): conflict-free float4 rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -212,14 +225,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // rank 1 of a pair issues no MMA
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], MC);  // one MMA commit from each CTA that reads the stage
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4 * 32);
+            mbar_init(&tempty[a], PAIR ? 2 * 4 : 4 * 32);  // pairs: one arrival per epilogue warp of each CTA
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -227,16 +241,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
-        prefetch_tensormap(MC > 1 ? &tmBp : &tmB);
+        prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        if constexpr (PAIR) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+        else tmem_alloc(tmem_slot, C::TMEM_COLS);
         tc_fence_before();
     }
     __syncthreads();
-    // peers multicast into this CTA's stages and arrive on its barriers: all barriers of
-    // the cluster are initialised before anyone issues a copy
-    if constexpr (MC > 1) cluster_sync();
+    // pairs: the peer arrives on this CTA's barriers, so both CTAs' barriers are
+    // initialised (and TMEM allocated) before either goes on
+    if constexpr (PAIR) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kblocks = args.kblocks;
@@ -245,9 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // come from the previous kernel.  Each such stage is armed for its full A + B byte
     // count now; its A tile follows once the wait returns.
     int n_pre = 0;
-    if constexpr (MC == 1) {
+    if constexpr (!PAIR) {
         TileId id0;
-        if (args.prefetch_b && warp == 0 && lane == 0 && tile_at<MC>(args, 0, id0)) {
+        if (args.prefetch_b && warp == 0 && lane == 0 && tile_at<PAIR>(args, 0, id0)) {
             const int kb0 = id0.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
             n_pre = min(C::STAGES, kb1 - kb0);
             for (int i = 0; i < n_pre; ++i) {
@@ -261,16 +276,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            const uint32_t leader_full = PAIR ? cluster_map(smem_u32(full), 0) : 0u;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed[C::STAGES];
             for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
             bool ok = true;
             TileId id;
-            for (int it = 0; ok && tile_at<MC>(args, it, id); ++it) {
+            for (int it = 0; ok && tile_at<PAIR>(args, it, id); ++it) {
                 const int a_row = id.mt >= args.n_mtiles ? args.a_rows
                                   : args.a_row_of_mtile ? args.a_row_of_mtile[id.mt] : id.mt * BM;
-                const int b_row = id.nt * BN;
+                const int b_row = id.nt * BN + int(rank) * C::B_ROWS;  // pairs: this CTA's half of B
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     const bool pre = n_pre > 0;  // stage armed and its B requested before the wait
@@ -281,17 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
+                        // pairs: rank 0's barrier counts the stage's bytes of both CTAs
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * (C::A_BYTES + C::B_BYTES));
                     }
-                    tma_load_2d(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, &full[stage]);
-                    if (!pre) {
-                        if constexpr (MC == 1) {
-                            tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
-                        } else {
-                            const int r = int(blockIdx.x) % MC;
-                            tma_load_2d_mc(sB + stage * C::B_BYTES + r * (C::B_BYTES / MC), &tmBp, kb * BK,
-                                           b_row + r * (BN / MC), &full[stage], kPeers);
-                        }
+                    if (PAIR && rank != 0) {
+                        const uint32_t bar = leader_full + 8u * uint32_t(stage);
+                        tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, bar);
+                        tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, bar);
+                    } else {
+                        tma_load_2d(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, &full[stage]);
+                        if (!pre) tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
                     }
                     ++armed[stage];
                     if (++stage == C::STAGES) {
@@ -300,24 +315,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {  // let every copy this thread started land before the CTA exits
+            if (!ok && rank == 0) {  // let every copy this CTA's barriers count land before it exits
                 for (int s = 0; s < C::STAGES; ++s)
                     if (armed[s] != 0) mbar_wait_bounded(&full[s], (armed[s] - 1) & 1u, nullptr, nullptr);
             }
         }
         __syncwarp();
+    } else if (warp == 1 && PAIR && rank != 0) {
+        // rank 1 of a pair issues no MMA
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
+            // pairs: the peer's empty / tfull barriers (same offsets in rank 1's shared memory)
+            const uint32_t peer_empty = PAIR ? cluster_map(smem_u32(empty), 1) : 0u;
+            const uint32_t peer_tfull = PAIR ? cluster_map(smem_u32(tfull), 1) : 0u;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
             TileId id;
-            for (int it = 0; ok && tile_at<MC>(args, it, id); ++it, ++local) {
+            for (int it = 0; ok && tile_at<PAIR>(args, it, id); ++it, ++local) {
                 const int acc = local & 1;
                 const uint32_t use = uint32_t(local >> 1);
-                if (!mbar_wait_bounded(&tempty[acc], (use & 1u) ^ 1u, abort_flag, args.dev_flags)) break;
+                if (!mbar_wait_bounded(&tempty[acc], (use & 1u) ^ 1u, abort_flag, args.dev_flags, kWaitLimitNs, PAIR))
+                    break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
@@ -331,29 +352,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
-                                    (kb > kb0 || k > 0) ? 1u : 0u);
+                        const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+                        if constexpr (PAIR)
+                            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
+                                             accum);
+                        else
+                            tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
+                                        accum);
                     }
-                    if constexpr (MC == 1) tc_commit(&empty[stage]);
-                    else tc_commit_mc(&empty[stage], kPeers);  // the stage is free once every CTA is done
+                    if constexpr (PAIR) {  // the stage is free in both CTAs once the MMAs are done
+                        tc_commit_pair(smem_u32(&empty[stage]));
+                        tc_commit_pair(peer_empty + 8u * uint32_t(stage));
+                    } else {
+                        tc_commit(&empty[stage]);
+                    }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) tc_commit(&tfull[acc]);
+                if (ok) {
+                    if constexpr (PAIR) {
+                        tc_commit_pair(smem_u32(&tfull[acc]));
+                        tc_commit_pair(peer_tfull + 8u * uint32_t(acc));
+                    } else {
+                        tc_commit(&tfull[acc]);
+                    }
+                }
             }
             // every MMA this thread issued completes before TMEM is released
-            tc_commit(drain);
+            if constexpr (PAIR) tc_commit_pair(smem_u32(drain));
+            else tc_commit(drain);
             mbar_wait_bounded(drain, 0, nullptr, args.dev_flags);
         }
         __syncwarp();
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may read
         const int r_in_tile = quarter * 32 + lane;
+        // pairs: rank 0's tempty barriers, where the epilogue warps of both CTAs arrive
+        const uint32_t leader_tempty = PAIR ? cluster_map(smem_u32(tempty), 0) : 0u;
         int local = 0;
         TileId id;
-        for (int it = 0; tile_at<MC>(args, it, id); ++it, ++local) {
+        for (int it = 0; tile_at<PAIR>(args, it, id); ++it, ++local) {
             const int acc = local & 1;
             const uint32_t use = uint32_t(local >> 1);
             // split-K: this thread's share of the tile's bias, read while the MMAs run
@@ -383,7 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r);
                 }
                 tc_fence_before();
-                mbar_arrive(&tempty[acc]);
+                if constexpr (PAIR) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(leader_tempty + 8u * uint32_t(acc));
+                } else {
+                    mbar_arrive(&tempty[acc]);
+                }
                 continue;
             }
             // split-K: stage this split's fp32 rows in shared memory.  The operand stages
@@ -410,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    if (args.splits > 1) {
+    if (!PAIR && args.splits > 1) {
         // every thread of every CTA of the cluster passes both barriers, on every path
         cluster_sync();
         if (warp >= 2) {
@@ -462,11 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // no CTA leaves while another may still read its shared memory
     }
     __syncthreads();
-    // no CTA leaves while a peer may still multicast into it or arrive on its barriers
-    if constexpr (MC > 1) cluster_sync();
+    // pairs: no CTA leaves (or frees TMEM) while rank 0's MMAs may still read its shared
+    // memory or write its TMEM, or while its peer may still arrive on its barriers
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -508,21 +555,21 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 namespace {
 
 // Opts the kernel into its dynamic shared memory size (once per instantiation).
-template <int BN, int MC>
+template <int BN, bool PAIR>
 cudaError_t kernel_attributes() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   GemmCfg<BN>::SMEM);
+        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   GemmCfg<BN, PAIR>::SMEM);
     });
     return err;
 }
 
 // How many clusters of `size` CTAs of this kernel the GPU holds at once (0: none).
-template <int BN, int MC>
+template <int BN, bool PAIR>
 int active_clusters(int size) {
-    if (kernel_attributes<BN, MC>() != cudaSuccess) return 0;
+    if (kernel_attributes<BN, PAIR>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -531,11 +578,11 @@ int active_clusters(int size) {
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(size);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = GemmCfg<BN>::SMEM;
+    cfg.dynamicSmemBytes = GemmCfg<BN, PAIR>::SMEM;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, MC>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, PAIR>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -550,7 +597,7 @@ int max_cluster_splits() {
     static int best = 1;
     std::call_once(once, [] {
         for (int S = kMaxSplits; S > 1; S >>= 1) {
-            if (active_clusters<BN, 1>(S) > 0) {
+            if (active_clusters<BN, false>(S) > 0) {
                 best = S;
                 break;
             }
@@ -559,30 +606,16 @@ int max_cluster_splits() {
     return best;
 }
 
-// Clusters of MC B-multicast CTAs the GPU holds at once (0: the mode is unavailable).
-template <int MC>
-int multicast_clusters() {
+// CTA pairs of the BN = 256 pair kernel the GPU holds at once (0: the mode is unavailable).
+int pair_clusters() {
     static std::once_flag once;
     static int n = 0;
-    std::call_once(once, [] { n = active_clusters<256, MC>(MC); });
+    std::call_once(once, [] { n = active_clusters<256, true>(2); });
     return n;
 }
 
-template <int BN, int MC>
-cudaError_t launch_multicast(const GemmProblem& p, const GemmArgs& a, int clusters, cudaStream_t s,
-                             const CUtensorMap& ta, const CUtensorMap& tb) {
-    if (kernel_attributes<BN, MC>() != cudaSuccess) return cudaErrorInvalidValue;
-    CUtensorMap tbp;
-    if (!make_tma_2d_bf16(&tbp, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN / MC))
-        return cudaErrorInvalidValue;
-    const int groups = (a.n_mtiles + MC - 1) / MC * a.n_ntiles;
-    const int grid = MC * std::min(groups, clusters);
-    return launch_cluster(gemm_tc_kernel<BN, MC>, grid, MC, GemmCfg<BN>::SMEM, s, ta, tb, tbp, a);
-}
-
-cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs), int grid, int cluster,
-                           size_t smem, cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tbp, const GemmArgs& a) {
+cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, GemmArgs), int grid, int cluster, size_t smem,
+                           cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a) {
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -597,17 +630,36 @@ cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap,
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return counted(cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbp, a));
+    return counted(cudaLaunchKernelEx(&cfg, kernel, ta, tb, a));
+}
+
+// Operand-heavy BN = 256 launches (more output tiles than SMs) run as CTA pairs: the
+// pair's 256 x 256 tile is one cta_group::2 MMA stream, and each CTA loads only its own
+// 128 A rows and 128 of the 256 B rows, which cuts the L2-to-SM operand traffic per K
+// block from 48 KB to 32 KB per CTA.  Returns false (nothing launched) when the GPU
+// cannot hold a pair of this kernel.
+bool launch_pair(const GemmProblem& p, const GemmArgs& a, cudaStream_t s, const CUtensorMap& ta, cudaError_t* err) {
+    using C = GemmCfg<256, true>;
+    const int clusters = pair_clusters();
+    if (clusters <= 0) return false;
+    CUtensorMap tbh;  // B in 128-row boxes: this CTA's half of the pair's B tile
+    if (!make_tma_2d_bf16(&tbh, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), C::B_ROWS)) {
+        *err = cudaErrorInvalidValue;
+        return true;
+    }
+    const int groups = (a.n_mtiles + 1) / 2 * a.n_ntiles;
+    const int grid = 2 * std::min(groups, clusters);
+    *err = launch_cluster(gemm_tc_kernel<256, true>, grid, 2, C::SMEM, s, ta, tbh, a);
+    return true;
 }
 
 template <int BN>
 cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s, int splits) {
-    using C = GemmCfg<BN>;
-    const cudaError_t attr_err = kernel_attributes<BN, 1>();
+    using C = GemmCfg<BN, false>;
+    const cudaError_t attr_err = kernel_attributes<BN, false>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ta, tb;
     if (!make_tma_2d_bf16(&ta, p.A, uint64_t(p.K), uint64_t(p.a_rows), uint64_t(p.lda), BM)) return cudaErrorInvalidValue;
-    if (!make_tma_2d_bf16(&tb, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN)) return cudaErrorInvalidValue;
     GemmArgs a;
     a.n_mtiles = p.n_mtiles;
     a.n_ntiles = p.N / BN;
@@ -622,17 +674,19 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     const int sms = num_sms();
     const int out_tiles = a.n_mtiles * a.n_ntiles;
     const int tiles = out_tiles * a.splits;
-    if (a.splits > 1)  // one CTA per (output tile, split); the splits of a tile form one cluster
-        return launch_cluster(gemm_tc_kernel<BN, 1>, tiles, a.splits, C::SMEM, s, ta, tb, tb, a);
     if constexpr (BN == 256) {
-        // Operand-heavy launches (more tiles than SMs): pairs of CTAs on neighbouring M
-        // tiles share each B tile, every CTA loading half of it for both, which cuts the
-        // L2-to-SM operand traffic by a third.
-        const int pairs = out_tiles > sms ? multicast_clusters<2>() : 0;
-        if (pairs > 0) return launch_multicast<BN, 2>(p, a, pairs, s, ta, tb);
+        if (a.splits == 1 && out_tiles > sms) {
+            a.prefetch_b = 0;
+            cudaError_t err = cudaSuccess;
+            if (launch_pair(p, a, s, ta, &err)) return err;
+            a.prefetch_b = p.b_is_weight ? 1 : 0;
+        }
     }
+    if (!make_tma_2d_bf16(&tb, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN)) return cudaErrorInvalidValue;
+    if (a.splits > 1)  // one CTA per (output tile, split); the splits of a tile form one cluster
+        return launch_cluster(gemm_tc_kernel<BN, false>, tiles, a.splits, C::SMEM, s, ta, tb, a);
     const int grid = tiles < sms ? tiles : sms;
-    return launch_pdl(gemm_tc_kernel<BN, 1>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, tb, a);
+    return launch_pdl(gemm_tc_kernel<BN, false>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, a);
 }
 
 }  // namespace
