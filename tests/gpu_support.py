@@ -73,6 +73,14 @@ def run_oracle(w, shape, bt, records=None, keep=False):
                                records=records, keep=keep)
 
 
+def rel_rms(got, ref):
+    """Root-mean-square error relative to the reference's RMS: a systematic slip in a
+    stage (a wrong bias, a skipped norm, a shifted row) moves it by O(1), where
+    per-element rounding of bf16 activations stays near 1e-3."""
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    return float(np.sqrt(((got - ref) ** 2).mean() / max((ref ** 2).mean(), 1e-30)))
+
+
 def compare(gpu, ref, bt, records=None):
     """Acceptance check on the options / questions of ``records`` (all by default)."""
     if records is None:

@@ -16,7 +16,7 @@ import synth
 from structured_decision_model_gb300 import binding as B
 from structured_decision_model_gb300.build import build_library
 
-from gpu_support import compare, device_inputs, head_for, run_gpu, run_oracle, schema_of
+from gpu_support import compare, device_inputs, head_for, rel_rms, run_gpu, run_oracle, schema_of
 
 pytestmark = pytest.mark.gpu
 
@@ -139,9 +139,45 @@ def test_pr1_reference_record_full_head():
     np.testing.assert_allclose(bufs["pooled_c"].cpu().numpy(), inter["c"], atol=2e-4)
     np.testing.assert_allclose(bufs["pooled_x"].cpu().numpy(), inter["x"], atol=1e-6)
     np.testing.assert_allclose(bufs["global_g"].cpu().numpy()[0], inter["g"], atol=2e-4)
-    np.testing.assert_allclose(bufs["option_final"].cpu().numpy(), inter["o_hat"], atol=5e-2)
-    np.testing.assert_allclose(bufs["field_final"].cpu().numpy(), inter["f_hat"], atol=5e-2)
+    o_hat, f_hat = bufs["option_final"].cpu().numpy(), bufs["field_final"].cpu().numpy()
+    print("option_final max", np.abs(o_hat - inter["o_hat"]).max(), "rel rms", rel_rms(o_hat, inter["o_hat"]))
+    print("field_final max", np.abs(f_hat - inter["f_hat"]).max(), "rel rms", rel_rms(f_hat, inter["f_hat"]))
+    # measured on GB300: max 0.014 / 0.012, relative RMS 0.0032 / 0.0032
+    np.testing.assert_allclose(o_hat, inter["o_hat"], atol=2.5e-2)
+    np.testing.assert_allclose(f_hat, inter["f_hat"], atol=2.5e-2)
+    assert rel_rms(o_hat, inter["o_hat"]) < 1e-2
+    assert rel_rms(f_hat, inter["f_hat"]) < 1e-2
     compare(gpu, ref, bt)
+
+
+def test_ln_fold_rows_with_offsets_and_outlier_channels():
+    """The memory LayerNorm is folded into the K/V projection as rstd * (h W'^T - mu c) + b',
+    which subtracts two large terms when a row's mean is large against its spread.
+    Final-norm hidden states have per-row offsets and a few outlier channels, so the
+    rows here get a mean drawn U(-4, 4) and six channels scaled by 30-50.  Pooled vectors
+    (which use the same statistics), the option stream after routing (which reads the
+    folded K/V) and the head outputs are compared with the oracle."""
+    spec = synth.BatchSpec(name="lnfold", B=2, lengths=[2304, 3001], questions=(4, 6), options=(2, 6))
+    bt = synth.make_batch(spec, seed=19)
+    rng = np.random.default_rng(19)
+    h = synth.bf16_to_f32(bt.hidden)
+    h += rng.uniform(-4, 4, size=(bt.B, bt.Lpad, 1)).astype(np.float32)
+    ch = rng.choice(bt.H, size=6, replace=False)
+    h[:, :, ch] *= rng.uniform(30, 50, size=6).astype(np.float32)
+    bt = dataclasses.replace(bt, hidden=synth.f32_to_bf16(h))
+    head, w = head_for(FULL)
+    bufs, dbg = _debug_buffers(bt, FULL)
+    gpu = run_gpu(head, bt, debug=dbg)
+    ref = run_oracle(w, FULL, bt, keep=True)
+    u = np.concatenate([ref["inter"][b]["u"] for b in range(bt.B)])
+    c = np.concatenate([ref["inter"][b]["c"] for b in range(bt.B)])
+    o_hat = np.concatenate([ref["inter"][b]["o_hat"] for b in range(bt.B)])
+    got_o = bufs["option_final"].cpu().numpy()
+    print("lnfold option_final max", np.abs(got_o - o_hat).max(), "rel rms", rel_rms(got_o, o_hat))
+    np.testing.assert_allclose(bufs["pooled_u"].cpu().numpy(), u, atol=2e-3, rtol=1e-3)
+    np.testing.assert_allclose(bufs["pooled_c"].cpu().numpy(), c, atol=2e-3, rtol=1e-3)
+    assert rel_rms(got_o, o_hat) < 1e-2
+    print("lnfold", compare(gpu, ref, bt))
 
 
 def ragged_spec(**kw):

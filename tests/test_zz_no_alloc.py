@@ -80,3 +80,45 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         for a, b in zip(*outs):
             assert np.isfinite(a).all()
             np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_out_of_range_token_id_then_recovers():
+    """An option token id outside the vocabulary is skipped by the pooling kernel and
+    returned directly as CLEF_ERR_DEVICE_BOUNDS (the call waits for its stream); the
+    other sums still equal the workspace entry's, and the next clean call returns OK,
+    because every call clears the status word in the shared array first."""
+    build_library()
+    B.load()
+    H, vocab = 256, 3000
+    cfg = B.make_config(H=H, vocab=vocab)
+    stream = torch.cuda.current_stream().cuda_stream
+    bt, table = _batch(23, 3, H, vocab)
+    sch = _schema(bt)
+    hidden = torch.from_numpy(bt.hidden.view(np.int16)).cuda().view(torch.bfloat16)
+    lex = torch.from_numpy(table.view(np.int16)).cuda().view(torch.bfloat16)
+    bad_ids = bt.token_ids.copy()
+    bad_ids[bt.q_rec[0], bt.o_span[0, 0]] = vocab + 7
+    outs = []
+    for ids_np, use_ws in ((bad_ids, True), (bad_ids, False)):
+        ids = torch.from_numpy(ids_np).cuda()
+        q, o, x = (torch.zeros((n, H), dtype=torch.float32, device="cuda") for n in (bt.Q, bt.O, bt.O))
+        if use_ws:
+            nws = B.clef_workspace_size(cfg, sch)
+            ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+            B.clef_span_sums(cfg, sch, hidden.data_ptr(), ids.data_ptr(), lex.data_ptr(), q.data_ptr(),
+                             o.data_ptr(), x.data_ptr(), ws.data_ptr(), nws, stream)
+            torch.cuda.synchronize()
+            assert B.clef_device_status(ws.data_ptr(), stream) == 5  # CLEF_ERR_DEVICE_BOUNDS
+        else:
+            st = B.clef_span_sums_noalloc(cfg, sch, hidden.data_ptr(), ids.data_ptr(), lex.data_ptr(),
+                                          q.data_ptr(), o.data_ptr(), x.data_ptr(), stream)
+            assert st == 5, B.STATUS.get(st, st)
+        outs.append([t.cpu().numpy() for t in (q, o, x)])
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+    ids = torch.from_numpy(bt.token_ids).cuda()
+    q, o, x = (torch.zeros((n, H), dtype=torch.float32, device="cuda") for n in (bt.Q, bt.O, bt.O))
+    st = B.clef_span_sums_noalloc(cfg, sch, hidden.data_ptr(), ids.data_ptr(), lex.data_ptr(), q.data_ptr(),
+                                  o.data_ptr(), x.data_ptr(), stream)
+    assert st == 0, B.STATUS.get(st, st)
