@@ -9,9 +9,11 @@ workload, inputs resident in HBM.  Default workload: 8 records of 16384 memory r
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead,
 on a bounded sample of the same workload (the only other place this file runs the
-oracle is the ``cpu_baseline`` leg).  Under torchrun every rank runs the same
-per-GPU batch (weak scaling, records are independent; no collective on the data
-path).
+oracle is the ``cpu_baseline`` leg).  Under torchrun the job holds one batch of
+N x 8 records of the same shape; ``shard_records`` gives every rank its own 8 (weak
+scaling: records are independent, so there is no collective on the data path) and
+each rank draws and uploads only its own records.  After the timed region the
+per-rank outputs are gathered once through ``ShardedRunner`` and checked.
 """
 import argparse
 import dataclasses
@@ -40,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum of one full K/V-projection launch of this
 # workload: an ncu capture of the same kernel on the first 2 records, scaled to 8 records
 # (set to None whenever the kernel changes until it is captured again).
-KV_GEMM_TRAFFIC_BYTES = 2.240e9
+KV_GEMM_TRAFFIC_BYTES = 2.265e9
 
 
 def load_peaks():
@@ -142,6 +144,17 @@ def oracle_one_record(w, shape, bt, b):
     return time.perf_counter() - t0
 
 
+def local_batch(bt_g, sb):
+    """The records of one shard as a batch of their own: tables re-indexed from zero,
+    padded to the shard's longest record, hidden rows drawn for these records only."""
+    recs = sb.records
+    Lp = int(sb.lengths.max())
+    hid = np.stack([bt_g.record_hidden(int(b))[:Lp] for b in recs])
+    return dataclasses.replace(bt_g, B=len(recs), Lpad=Lp, lengths=sb.lengths, q_rec=sb.q_rec, q_type=sb.q_type,
+                               q_span=sb.q_span, q_opt_off=sb.q_opt_off, o_span=sb.o_span,
+                               token_ids=np.ascontiguousarray(bt_g.token_ids[recs, :Lp]), hidden=hid)
+
+
 def run_reference(args, spec, shape):
     """The oracle as it stands, timed on the host cores: one step = one record."""
     rank = int(os.environ.get("RANK", "0"))
@@ -206,6 +219,7 @@ def main():
     from structured_decision_model_gb300 import binding as B
     from structured_decision_model_gb300.build import build_library
     from structured_decision_model_gb300.head import ClefHead, to_device_bf16
+    from structured_decision_model_gb300.sharding import ShardedRunner, shard_records, sub_batch
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -219,8 +233,15 @@ def main():
     build_library()
     B.load()
 
-    # every rank: its own seeded batch of the same workload (weak scaling)
-    bt = synth.make_batch(spec, seed=1 + rank)
+    # one batch of world x B records; this rank's shard (B records, weak scaling) is
+    # picked by the same row-balanced split ShardedRunner uses
+    spec_g = spec if world == 1 else dataclasses.replace(
+        spec, B=spec.B * world, lengths=None if spec.lengths is None else list(spec.lengths) * world)
+    bt_g = synth.make_batch(spec_g, seed=1, with_hidden=(world == 1))
+    tables = (bt_g.lengths, bt_g.q_rec, bt_g.q_type, bt_g.q_span, bt_g.q_opt_off, bt_g.o_span)
+    shards = shard_records(bt_g.lengths, world)
+    sb = sub_batch(shards[rank], *tables)
+    bt = bt_g if world == 1 else local_batch(bt_g, sb)
     w = synth.make_weights(shape, seed=0)
     head = ClefHead(w, shape.H, shape.D, shape.heads, shape.F, shape.n_route, shape.n_joint, shape.vocab, device=dev)
     schema = B.Schema(bt.B, bt.Lpad, bt.H, bt.lengths, bt.q_rec, bt.q_type, bt.q_span, bt.q_opt_off, bt.o_span)
@@ -368,13 +389,27 @@ def main():
                        "ingest_ms": s0.elapsed_time(s1), "host_us_per_chunk": t_host * 1e6 / len(chunks),
                        "forward_ms": ms}
 
+    # the gather of the sharded runner: every rank's outputs, once, after the timed
+    # region; checked against this rank's own outputs (a few KB per rank)
+    sharded = None
+    if world > 1:
+        mine = {"logits": out.logits.cpu().numpy(), "probs": out.probs.cpu().numpy(),
+                "value": out.q_value.cpu().numpy(), "conf": out.q_conf.cpu().numpy(),
+                "argmax": out.q_argmax.cpu().numpy()}
+        full = ShardedRunner(lambda _sb: mine).forward(*tables)
+        ok = bool(np.array_equal(full["logits"][sb.o_index], mine["logits"]) and np.isfinite(full["logits"]).all())
+        sharded = {"records_total": int(bt_g.B), "records_per_rank": [len(x) for x in shards], "gather_ok": ok}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b0 = 0
-        dt = oracle_one_record(w, shape, bt, b0)
+        recs = list(range(min(3, bt.B)))
+        dts = [oracle_one_record(w, shape, bt, b) for b in recs]
+        dt = statistics.median(dts)
         cpu = {"value": 1.0 / dt, "unit": "records/s", "cores": NCPU, "kind": "oracle",
-               "sample": f"record 0 of the batch ({int(bt.lengths[b0])} memory rows, {int((bt.q_rec == b0).sum())} "
-                         f"questions), fp64 NumPy, {dt:.1f} s"}
+               "sample": f"records {recs} of the batch ({int(bt.lengths[0])} memory rows, "
+                         f"{int((bt.q_rec == 0).sum())} questions each), one record per timing, median of "
+                         f"{len(recs)}; the oracle is fp64 NumPy (slower than an fp32 program would be), "
+                         f"{sum(dts):.1f} s in total"}
 
     if rank == 0:
         peaks, peak_src = load_peaks()
@@ -411,6 +446,7 @@ def main():
                     "timing": "host wall clock around e2e steps, input copies double-buffered on a copy stream"},
             "gpu_launches": int(launches),
             "stream": stream_info,
+            "sharded": sharded,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))

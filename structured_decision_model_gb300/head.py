@@ -115,3 +115,33 @@ class ClefHead:
 
     def device_status(self, stream=None) -> int:
         return B.clef_device_status(self._ws.data_ptr(), stream_handle(stream))
+
+    def shard_fn(self, hidden, token_ids, lexical: torch.Tensor, stream=None):
+        """The per-rank compute of ``sharding.ShardedRunner``: the shard's records
+        through this GPU's head.
+
+        ``hidden`` [B, Lpad, H] bf16 and ``token_ids`` [B, Lpad] int32 hold the whole
+        batch, as torch tensors on any device or as numpy arrays on the host (bf16 as
+        uint16 bit patterns); only the shard's records, up to the shard's longest
+        length, are copied to this GPU.  ``lexical`` is this GPU's copy of the table.
+        Raises if the device reports an error."""
+        def run(sb) -> dict:
+            Lp = int(sb.lengths.max())
+            if isinstance(hidden, np.ndarray):
+                h = to_device_bf16(hidden[sb.records, :Lp], self.device)
+            else:
+                h = hidden[torch.as_tensor(sb.records, device=hidden.device), :Lp].to(self.device).contiguous()
+            if isinstance(token_ids, np.ndarray):
+                ids = torch.from_numpy(np.ascontiguousarray(token_ids[sb.records, :Lp], np.int32)).to(self.device)
+            else:
+                ids = token_ids[torch.as_tensor(sb.records, device=token_ids.device), :Lp].to(self.device).contiguous()
+            schema = B.Schema(len(sb.records), Lp, self.H, sb.lengths, sb.q_rec, sb.q_type, sb.q_span, sb.q_opt_off,
+                              sb.o_span)
+            out = self.forward(schema, h, ids, lexical, stream=stream)
+            st = self.device_status(stream)  # waits for the stream
+            if st != 0:
+                raise B.ClefError(st, "device status after a shard")
+            return {"logits": out.logits.cpu().numpy(), "probs": out.probs.cpu().numpy(),
+                    "value": out.q_value.cpu().numpy(), "conf": out.q_conf.cpu().numpy(),
+                    "argmax": out.q_argmax.cpu().numpy()}
+        return run
