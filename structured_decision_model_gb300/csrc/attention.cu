@@ -6,13 +6,14 @@
 // option queries of that record); only the blocks a record needs are listed.  The
 // kernel is persistent: each CTA walks work w = blockIdx.x + i * gridDim.x (head
 // fastest, so CTAs running side by side read the same memory rows).  A producer warp
-// streams 64-row K and V tiles with TMA (128-byte swizzle) through a 3-stage mbarrier
+// streams 64-row K and V tiles with TMA (128-byte swizzle) through a 4-stage mbarrier
 // ring that runs on from one work item to the next, and loads each item's queries
-// into one of two query slots, so the next item's data arrive while the current one
-// finishes.  Four consumer warps each own 16 queries and run QK^T and PV on mma.sync
-// bf16 tensor cores with an fp32 online softmax in the exp2 domain.  Keys at or past
-// the chunk end are masked.  Every (option, head, chunk) leaves (running max, running
-// sum, unnormalised accumulator); the merge kernel rescales and sums the chunks.
+// into the query slot as soon as the consumers have copied the previous item's
+// queries into registers.  Four consumer warps each own 16 queries and run QK^T and
+// PV on mma.sync bf16 tensor cores with an fp32 online softmax in the exp2 domain.
+// Keys at or past the chunk end are masked.  Every (option, head, chunk) leaves
+// (running max, running sum, unnormalised accumulator); the merge kernel rescales and
+// sums the chunks.
 // Every mbarrier wait is bounded; on a timeout the CTA flags it and returns.
 #include <algorithm>
 #include <mutex>
@@ -26,11 +27,12 @@ namespace clef {
 namespace {
 
 constexpr int kKT = 64;                     // keys per tile
-constexpr int kStages = 3;
+constexpr int kStages = 4;
+constexpr int kQSlots = 1;                  // query slots: the consumers hold an item's queries in registers
 constexpr int kQRows = kAttnQRows;          // option queries per work item (4 consumer warps x 16)
 constexpr int kTileBytes = kKT * 128;       // [64 rows][64 bf16]
 constexpr int kQBytes = kQRows * 128;
-constexpr int kSmem = 2 * kQBytes + kStages * 2 * kTileBytes + 1024 + 128;
+constexpr int kSmem = kQSlots * kQBytes + kStages * 2 * kTileBytes + 1024 + 128;
 constexpr int kThreads = 160;               // 4 consumer warps + 1 producer warp
 constexpr int kBlocksPerSM = 3;
 
@@ -71,13 +73,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     griddep_launch();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;                  // two query slots
-    uint8_t* sKV = smem + 2 * kQBytes;   // stage s: K at s * 2 * kTileBytes, V right after
+    uint8_t* sQ = smem;                        // query slots
+    uint8_t* sKV = smem + kQSlots * kQBytes;   // stage s: K at s * 2 * kTileBytes, V right after
     uint64_t* full = reinterpret_cast<uint64_t*>(sKV + kStages * 2 * kTileBytes);
     uint64_t* empty = full + kStages;
-    uint64_t* qfull = empty + kStages;   // [2]
-    uint64_t* qempty = qfull + 2;        // [2]
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(qempty + 2);
+    uint64_t* qfull = empty + kStages;
+    uint64_t* qempty = qfull + kQSlots;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(qempty + kQSlots);
 
     const int n_work = a.n_units * a.heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 4);
         }
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kQSlots; ++q) {
             mbar_init(&qfull[q], 1);
             mbar_init(&qempty[q], 4);
         }
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             prefetch_tensormap(&tmQ);
             prefetch_tensormap(&tmKV);
             uint32_t armed[kStages] = {};
-            uint32_t armed_q[2] = {};
+            uint32_t armed_q[kQSlots] = {};
             int stage = 0, qs = 0;
             uint32_t phase = 0, qphase = 0;
             bool ok = true;
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 mbar_arrive_expect_tx(&qfull[qs], kQBytes);
                 tma_load_2d(sQ + qs * kQBytes, &tmQ, k.h * 64, k.o_base + k.qp * kQRows, &qfull[qs]);
                 ++armed_q[qs];
-                if (++qs == 2) {
+                if (++qs == kQSlots) {
                     qs = 0;
                     qphase ^= 1u;
                 }
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 }
             }
             // every copy this thread started lands before the CTA can exit
-            for (int q = 0; q < 2; ++q)
+            for (int q = 0; q < kQSlots; ++q)
                 if (armed_q[q]) mbar_wait_bounded(&qfull[q], (armed_q[q] - 1) & 1u, nullptr, nullptr);
             for (int s = 0; s < kStages; ++s)
                 if (armed[s]) mbar_wait_bounded(&full[s], (armed[s] - 1) & 1u, nullptr, nullptr);
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[qs]);  // the queries are in registers
-        if (++qs == 2) {
+        if (++qs == kQSlots) {
             qs = 0;
             qphase ^= 1u;
         }
@@ -243,12 +245,16 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 nm[0] = -m_r[0];
                 nm[1] = -m_r[1];
                 uint32_t pa[4][4];
+                // p = 2^(s * scale - m), the exponent rounded to bf16 and raised two at a time
+                // on the bf16x2 path: P feeds the bf16 P V product either way, and a rounding
+                // of the exponent by 2^-9 relative changes p by at most about 7e-4 of the row
+                // maximum (it grows with |s - m| while p shrinks as 2^-|s - m|)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float p0 = ex2_approx(fmaf(s[j][0], sl2, nm[0])), p1 = ex2_approx(fmaf(s[j][1], sl2, nm[0]));
-                    const float p2 = ex2_approx(fmaf(s[j][2], sl2, nm[1])), p3 = ex2_approx(fmaf(s[j][3], sl2, nm[1]));
-                    pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
-                    pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+                    pa[j >> 1][(j & 1) * 2 + 0] =
+                        ex2_bf16x2(pack_bf16(fmaf(s[j][0], sl2, nm[0]), fmaf(s[j][1], sl2, nm[0])));
+                    pa[j >> 1][(j & 1) * 2 + 1] =
+                        ex2_bf16x2(pack_bf16(fmaf(s[j][2], sl2, nm[1]), fmaf(s[j][3], sl2, nm[1])));
                 }
                 constexpr uint32_t kOnes = 0x3F803F80u;  // two bf16 1.0
 #pragma unroll

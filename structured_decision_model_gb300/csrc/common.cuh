@@ -55,6 +55,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// 2^x for two bf16 values at once (bf16x2 in, bf16x2 out; -inf gives 0).
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 __device__ __forceinline__ float gelu_exact(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
