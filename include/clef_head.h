@@ -213,6 +213,26 @@ CLEF_API int clef_stream_finish(const clef_config* cfg, const void* const* weigh
                                 float* q_conf, int32_t* q_argmax, void* workspace, size_t workspace_bytes,
                                 const clef_debug_outputs* debug, void* stream);
 
+/* Streaming ingestion of fp16 hidden rows ("clef-flash-CoreAI metadata.json"
+ * decision.readout: the chunked graph hands over 64-position chunks of fp16 hidden
+ * rows).  Same arguments, layout and rules as clef_stream_rows / clef_stream_finish,
+ * but `hidden` holds IEEE fp16 values instead of bf16.  Every fp16 value is rounded to
+ * bf16 (round to nearest even) where the head reads it -- the memory statistics, the
+ * K/V projection and the span pooling -- so the outputs equal those of the bf16 calls
+ * on the rounded rows, bit for bit.  clef_stream_rows_f16 rounds a chunk through a
+ * staging area inside the workspace, at most 1024 rows per pass; it needs no extra
+ * workspace beyond clef_workspace_size.  The two entry points pair with each other:
+ * a batch whose rows came in as fp16 is finished with clef_stream_finish_f16, which
+ * reads `hidden` (fp16) again for the pooled spans and the global row. */
+CLEF_API int clef_stream_rows_f16(const clef_config* cfg, const void* prepared, const clef_schema* schema,
+                                  const uint16_t* hidden, int32_t record, int32_t row0, int32_t n_rows,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+CLEF_API int clef_stream_finish_f16(const clef_config* cfg, const void* const* weights, const void* prepared,
+                                    const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
+                                    const uint16_t* lexical, float* logits, float* probs, float* q_value,
+                                    float* q_conf, int32_t* q_argmax, void* workspace, size_t workspace_bytes,
+                                    const clef_debug_outputs* debug, void* stream);
+
 /* Waits for `stream`, then reads and clears the device-side status word kept at the
  * start of `workspace`: CLEF_OK, CLEF_ERR_DEVICE_BOUNDS or CLEF_ERR_DEVICE_TIMEOUT.
  * Every clef_head_forward / clef_span_sums call clears that word when it starts, so

@@ -21,7 +21,8 @@ EXPORTED = [
     "clef_weight_count", "clef_prepared_size", "clef_prepare_weights", "clef_workspace_size",
     "clef_head_forward", "clef_device_status", "clef_span_sums", "clef_gemm_bf16",
     "clef_kernel_launches", "clef_status_string", "clef_span_sums_noalloc", "clef_stream_begin",
-    "clef_stream_rows", "clef_stream_finish", "clef_selftest_wait_timeout",
+    "clef_stream_rows", "clef_stream_finish", "clef_selftest_wait_timeout", "clef_stream_rows_f16",
+    "clef_stream_finish_f16",
 ]
 
 _i32, _i64, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
@@ -75,6 +76,8 @@ def load():
     lib.clef_stream_rows.argtypes = [ctypes.POINTER(ClefConfig), _vp, ctypes.POINTER(ClefSchema), _vp, _i32, _i32,
                                      _i32, _vp, _sz, _vp]
     lib.clef_stream_finish.argtypes = lib.clef_head_forward.argtypes
+    lib.clef_stream_rows_f16.argtypes = lib.clef_stream_rows.argtypes
+    lib.clef_stream_finish_f16.argtypes = lib.clef_head_forward.argtypes
     lib.clef_span_sums.argtypes = [ctypes.POINTER(ClefConfig), ctypes.POINTER(ClefSchema), _vp, _vp, _vp, _vp, _vp,
                                    _vp, _vp, _sz, _vp]
     lib.clef_gemm_bf16.argtypes = [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp]
@@ -179,6 +182,26 @@ def clef_stream_finish(cfg, weight_ptrs, prepared_ptr, schema: Schema, hidden_pt
     _check(load().clef_stream_finish(ctypes.byref(cfg), arr, prepared_ptr, ctypes.byref(schema.struct), hidden_ptr,
                                      token_ids_ptr, lexical_ptr, logits_ptr, probs_ptr, q_value_ptr, q_conf_ptr,
                                      q_argmax_ptr, workspace_ptr, workspace_bytes, dbg, stream), "clef_stream_finish")
+
+
+def clef_stream_rows_f16(cfg, prepared_ptr, schema: Schema, hidden_ptr, record, row0, n_rows, workspace_ptr,
+                         workspace_bytes, stream=0, check=True):
+    st = load().clef_stream_rows_f16(ctypes.byref(cfg), prepared_ptr, ctypes.byref(schema.struct), hidden_ptr, record,
+                                     row0, n_rows, workspace_ptr, workspace_bytes, stream)
+    if check:
+        _check(st, "clef_stream_rows_f16")
+    return st
+
+
+def clef_stream_finish_f16(cfg, weight_ptrs, prepared_ptr, schema: Schema, hidden_ptr, token_ids_ptr, lexical_ptr,
+                           logits_ptr, probs_ptr, q_value_ptr, q_conf_ptr, q_argmax_ptr, workspace_ptr,
+                           workspace_bytes, debug=None, stream=0):
+    arr = (_vp * len(weight_ptrs))(*weight_ptrs)
+    dbg = ctypes.byref(debug) if debug is not None else None
+    _check(load().clef_stream_finish_f16(ctypes.byref(cfg), arr, prepared_ptr, ctypes.byref(schema.struct),
+                                         hidden_ptr, token_ids_ptr, lexical_ptr, logits_ptr, probs_ptr, q_value_ptr,
+                                         q_conf_ptr, q_argmax_ptr, workspace_ptr, workspace_bytes, dbg, stream),
+           "clef_stream_finish_f16")
 
 
 def clef_kernel_launches():

@@ -16,6 +16,7 @@ using namespace clef;
 namespace {
 
 constexpr int kTile = 128;  // rows per GEMM output tile; records are padded to it in compact row space
+constexpr int kStageRows = 1024;  // fp16 streaming: rows rounded to bf16 per staging pass
 
 bool config_ok(const clef_config* c) {
     if (!c) return false;
@@ -259,7 +260,7 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
 
 struct WsLayout {
     size_t flags, plan, mu, rstd, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf,
-        q_buf, attn_buf, hid_buf, o_hat, f_res, f_hat, z, pm, pl, pacc, total;
+        q_buf, attn_buf, hid_buf, o_hat, f_res, f_hat, z, pm, pl, pacc, stage, total;
     WsLayout(const clef_config* c, const Plan& p) {
         const size_t H = c->hidden, D = c->width, F = c->ffn, NKV = size_t(2) * c->n_route * D;
         const size_t B = p.B, Q = p.Q, O = p.O, R = p.R, MQO = std::max(Q, O);
@@ -286,6 +287,7 @@ struct WsLayout {
         pm = cv.take(size_t(p.P) * 4);
         pl = cv.take(size_t(p.P) * 4);
         pacc = cv.take(size_t(p.P) * 64 * 4);
+        stage = cv.take(size_t(kStageRows) * H * 2);  // bf16 copy of fp16 streamed rows
         total = cv.off;
     }
 };
@@ -422,8 +424,9 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
                  const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
                  const uint16_t* lexical, float* logits, float* probs, float* q_value, float* q_conf,
                  int32_t* q_argmax, void* workspace, size_t workspace_bytes, const clef_debug_outputs* debug,
-                 void* stream, int mode) {
+                 void* stream, int mode, bool hidden_f16 = false) {
     if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (hidden_f16 && mode != kForwardAfterStream) return CLEF_ERR_INVALID_ARGUMENT;
     if (!weights || !prepared || !hidden || !token_ids || !lexical || !logits || !probs || !q_value || !q_conf ||
         !q_argmax || !workspace)
         return CLEF_ERR_INVALID_ARGUMENT;
@@ -500,6 +503,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     sp.u32 = u32; sp.x32 = x32; sp.g32 = g32;
     sp.dbg_c = debug ? debug->pooled_c : nullptr;
     sp.flags = flags;
+    sp.in_f16 = hidden_f16 ? 1 : 0;
     CK(mark(debug, 4, st));
     CK(launch_span_pool(sp, p.n_items, false, st)); CK(tick());
     CK(mark(debug, 5, st));
@@ -617,6 +621,61 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     return CLEF_OK;
 }
 
+// Statistics and K/V of rows [row0, row0 + n_rows) of one record.  fp16 rows are first
+// rounded to bf16 into the workspace staging area, kStageRows at a time; the statistics
+// and the projection then read that copy, exactly as they read bf16 rows.
+int stream_rows_impl(const clef_config* cfg, const void* prepared, const clef_schema* schema, const uint16_t* hidden,
+                     int32_t record, int32_t row0, int32_t n_rows, void* workspace, size_t workspace_bytes,
+                     void* stream, bool f16) {
+    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
+    if (!prepared || !hidden || !workspace || (reinterpret_cast<uintptr_t>(hidden) & 15) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(prepared) & 255))
+        return CLEF_ERR_INVALID_ARGUMENT;
+    const int v = validate_schema(cfg, schema);
+    if (v != CLEF_OK) return v;
+    if (record < 0 || record >= schema->B || row0 < 0 || n_rows < 1 ||
+        int64_t(row0) + n_rows > schema->lengths[record])
+        return CLEF_ERR_INVALID_ARGUMENT;
+    Plan p;
+    build_plan(cfg, schema, p);
+    const WsLayout L(cfg, p);
+    if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* pw = static_cast<const uint8_t*>(prepared);
+    const PreparedLayout PL(cfg);
+    const int H = cfg->hidden, NKV = 2 * cfg->n_route * cfg->width;
+    const int64_t out_row0 = p.blob[p.rec_row_off + record] + int64_t(row0);  // compact row of the first row
+    const uint16_t* rows0 = hidden + (int64_t(record) * schema->Lpad + row0) * schema->row_stride;
+    uint16_t* stage = reinterpret_cast<uint16_t*>(ws + L.stage);
+    for (int done = 0; done < n_rows;) {
+        const int n = f16 ? std::min(n_rows - done, kStageRows) : n_rows;
+        const uint16_t* rows = rows0 + int64_t(done) * schema->row_stride;
+        int64_t ld = schema->row_stride;
+        if (f16) {
+            CK(launch_f16_rows_to_bf16(rows, ld, n, H, stage, st));
+            rows = stage;
+            ld = H;
+        }
+        const int64_t out_row = out_row0 + done;
+        float* mu = reinterpret_cast<float*>(ws + L.mu) + out_row;
+        float* rstd = reinterpret_cast<float*>(ws + L.rstd) + out_row;
+        CK(launch_row_stats_rows(rows, ld, H, n, mu, rstd, st));
+        GemmProblem g;
+        g.A = rows; g.lda = ld; g.a_rows = n;
+        g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
+        g.N = NKV; g.K = H; g.n_mtiles = (n + kTile - 1) / kTile;
+        GemmEpilogue e;
+        e.kind = EPI_KV_LNFOLD; e.row_mu = mu; e.row_rstd = rstd;
+        e.col_c = reinterpret_cast<const float*>(pw + PL.ckv);
+        e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
+        e.out = reinterpret_cast<uint16_t*>(ws + L.kv) + out_row * NKV; e.ldo = NKV; e.M = n;
+        CK(launch_gemm(g, e, reinterpret_cast<int*>(ws + L.flags), st));
+        done += n;
+    }
+    return CLEF_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -647,40 +706,15 @@ int clef_stream_begin(const clef_config* cfg, const clef_schema* schema, void* w
 int clef_stream_rows(const clef_config* cfg, const void* prepared, const clef_schema* schema, const uint16_t* hidden,
                      int32_t record, int32_t row0, int32_t n_rows, void* workspace, size_t workspace_bytes,
                      void* stream) {
-    if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
-    if (!prepared || !hidden || !workspace || (reinterpret_cast<uintptr_t>(hidden) & 15) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(prepared) & 255))
-        return CLEF_ERR_INVALID_ARGUMENT;
-    const int v = validate_schema(cfg, schema);
-    if (v != CLEF_OK) return v;
-    if (record < 0 || record >= schema->B || row0 < 0 || n_rows < 1 ||
-        int64_t(row0) + n_rows > schema->lengths[record])
-        return CLEF_ERR_INVALID_ARGUMENT;
-    Plan p;
-    build_plan(cfg, schema, p);
-    const WsLayout L(cfg, p);
-    if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const uint8_t* pw = static_cast<const uint8_t*>(prepared);
-    const PreparedLayout PL(cfg);
-    const int H = cfg->hidden, NKV = 2 * cfg->n_route * cfg->width;
-    const int64_t out_row = p.blob[p.rec_row_off + record] + int64_t(row0);  // compact row of the first row
-    const uint16_t* rows = hidden + (int64_t(record) * schema->Lpad + row0) * schema->row_stride;
-    float* mu = reinterpret_cast<float*>(ws + L.mu) + out_row;
-    float* rstd = reinterpret_cast<float*>(ws + L.rstd) + out_row;
-    CK(launch_row_stats_rows(rows, schema->row_stride, H, n_rows, mu, rstd, st));
-    GemmProblem g;
-    g.A = rows; g.lda = schema->row_stride; g.a_rows = n_rows;
-    g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
-    g.N = NKV; g.K = H; g.n_mtiles = (n_rows + kTile - 1) / kTile;
-    GemmEpilogue e;
-    e.kind = EPI_KV_LNFOLD; e.row_mu = mu; e.row_rstd = rstd;
-    e.col_c = reinterpret_cast<const float*>(pw + PL.ckv);
-    e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
-    e.out = reinterpret_cast<uint16_t*>(ws + L.kv) + out_row * NKV; e.ldo = NKV; e.M = n_rows;
-    CK(launch_gemm(g, e, reinterpret_cast<int*>(ws + L.flags), st));
-    return CLEF_OK;
+    return stream_rows_impl(cfg, prepared, schema, hidden, record, row0, n_rows, workspace, workspace_bytes, stream,
+                            false);
+}
+
+int clef_stream_rows_f16(const clef_config* cfg, const void* prepared, const clef_schema* schema,
+                         const uint16_t* hidden, int32_t record, int32_t row0, int32_t n_rows, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    return stream_rows_impl(cfg, prepared, schema, hidden, record, row0, n_rows, workspace, workspace_bytes, stream,
+                            true);
 }
 
 int clef_stream_finish(const clef_config* cfg, const void* const* weights, const void* prepared,
@@ -690,6 +724,15 @@ int clef_stream_finish(const clef_config* cfg, const void* const* weights, const
                        void* stream) {
     return forward_impl(cfg, weights, prepared, schema, hidden, token_ids, lexical, logits, probs, q_value, q_conf,
                         q_argmax, workspace, workspace_bytes, debug, stream, kForwardAfterStream);
+}
+
+int clef_stream_finish_f16(const clef_config* cfg, const void* const* weights, const void* prepared,
+                           const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
+                           const uint16_t* lexical, float* logits, float* probs, float* q_value, float* q_conf,
+                           int32_t* q_argmax, void* workspace, size_t workspace_bytes,
+                           const clef_debug_outputs* debug, void* stream) {
+    return forward_impl(cfg, weights, prepared, schema, hidden, token_ids, lexical, logits, probs, q_value, q_conf,
+                        q_argmax, workspace, workspace_bytes, debug, stream, kForwardAfterStream, true);
 }
 
 int clef_device_status(void* workspace, void* stream) {

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,6 +47,16 @@ __device__ __forceinline__ float bf16_to_float(uint16_t v) { return __uint_as_fl
 __device__ __forceinline__ uint16_t float_to_bf16(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// Two fp16 values (one 32-bit word) rounded to two bf16 values (round to nearest even).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    return pack_bf16(f.x, f.y);
+}
+
+__device__ __forceinline__ uint4 f16x8_to_bf16x8(uint4 v) {
+    return make_uint4(f16x2_to_bf16x2(v.x), f16x2_to_bf16x2(v.y), f16x2_to_bf16x2(v.z), f16x2_to_bf16x2(v.w));
 }
 
 // 2^x with the hardware approximation instruction (about 2 ulp; -inf gives 0).

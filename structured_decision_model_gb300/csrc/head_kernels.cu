@@ -84,6 +84,21 @@ __global__ void __launch_bounds__(256) row_stats_rows_kernel(const uint16_t* __r
     }
 }
 
+// fp16 rows [rows][H] (row stride ld_src) rounded to a dense bf16 copy [rows][H]: the
+// streaming path's fp16 input, 8 values (16 bytes) per thread.
+__global__ void __launch_bounds__(256) f16_rows_to_bf16_kernel(const uint16_t* __restrict__ src, int64_t ld_src,
+                                                              int rows, int H, uint16_t* __restrict__ dst) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int c8 = H >> 3;
+    if (i >= int64_t(rows) * c8) return;
+    const int64_t r = i / c8;
+    const int c = int(i % c8);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + r * ld_src) + c);
+    reinterpret_cast<uint4*>(dst + r * H)[c] = f16x8_to_bf16x8(v);
+}
+
 // Zeroes K/V rows L_b .. roundup(L_b, 128) - 1 of every record (one CTA per record).
 __global__ void __launch_bounds__(256) zero_slack_kernel(uint16_t* __restrict__ kv, int ldkv,
                                                         const int32_t* __restrict__ rec_row_off,
@@ -108,9 +123,11 @@ __global__ void __launch_bounds__(256) zero_slack_kernel(uint16_t* __restrict__ 
 // LN(h_t) = (h_t - mu_t) * rstd_t * gamma + beta; the mean of the normalised rows is
 // taken first and the affine part applied once.  Each thread owns 8 columns per
 // step (one 16-byte load per row).  RAW = true writes plain span sums of the raw
-// rows instead (the bit-exact index check).
+// rows instead (the bit-exact index check).  F16 = true reads fp16 hidden rows and
+// rounds each value to bf16 first, so that pooling sees the same rows as the K/V
+// projection of the fp16 streaming path.
 // =====================================================================
-template <bool RAW>
+template <bool RAW, bool F16>
 __global__ void __launch_bounds__(256, 3) span_pool_kernel(SpanPoolArgs a) {
     griddep_wait();
     griddep_launch();
@@ -140,6 +157,7 @@ __global__ void __launch_bounds__(256, 3) span_pool_kernel(SpanPoolArgs a) {
             for (int u = 0; u < 6; ++u) {
                 if (u < nr) {
                     w[u] = __ldg(reinterpret_cast<const uint4*>(a.hidden + (rec_base + t0 + u) * a.row_stride) + c8);
+                    if (F16) w[u] = f16x8_to_bf16x8(w[u]);
                     if (!RAW) { m[u] = a.mu[stat_base + t0 + u]; rs[u] = a.rstd[stat_base + t0 + u]; }
                 }
             }
@@ -673,8 +691,20 @@ cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off
 
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s) {
     if (n_items <= 0) return cudaSuccess;
-    if (raw) return launch_pdl(span_pool_kernel<true>, dim3(n_items), dim3(256), 0, s, a);
-    return launch_pdl(span_pool_kernel<false>, dim3(n_items), dim3(256), 0, s, a);
+    if (a.in_f16) {
+        if (raw) return launch_pdl(span_pool_kernel<true, true>, dim3(n_items), dim3(256), 0, s, a);
+        return launch_pdl(span_pool_kernel<false, true>, dim3(n_items), dim3(256), 0, s, a);
+    }
+    if (raw) return launch_pdl(span_pool_kernel<true, false>, dim3(n_items), dim3(256), 0, s, a);
+    return launch_pdl(span_pool_kernel<false, false>, dim3(n_items), dim3(256), 0, s, a);
+}
+
+cudaError_t launch_f16_rows_to_bf16(const uint16_t* src, int64_t ld_src, int rows, int H, uint16_t* dst,
+                                    cudaStream_t s) {
+    const int64_t n = int64_t(rows) * (H / 8);
+    if (n <= 0) return cudaSuccess;
+    return launch_pdl(f16_rows_to_bf16_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, s, src, ld_src, rows,
+                      H, dst);
 }
 
 cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,

@@ -29,6 +29,7 @@ struct SpanPoolArgs {
     // raw-sum mode
     float* q_sum; float* o_sum; float* x_sum;
     int* flags;
+    int in_f16;                           // hidden rows are fp16 (rounded to bf16 when read)
 };
 
 struct RouteAttnArgs {
@@ -76,6 +77,8 @@ cudaError_t launch_wait_timeout_selftest(int* flags, uint64_t limit_ns, cudaStre
 cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off, const int32_t* lengths, int B,
                               cudaStream_t s);
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s);
+cudaError_t launch_f16_rows_to_bf16(const uint16_t* src, int64_t ld_src, int rows, int H, uint16_t* dst,
+                                    cudaStream_t s);
 cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
                               uint16_t* out_bf16, float* out_f32, cudaStream_t s);
 cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int O,

@@ -99,18 +99,22 @@ class ClefHead:
         B.clef_stream_begin(self.cfg, schema, ws.data_ptr(), ws.numel(), stream_handle(stream))
 
     def stream_rows(self, schema: B.Schema, hidden: torch.Tensor, record: int, row0: int, n_rows: int, stream=None):
+        """Statistics and K/V of rows [row0, row0 + n_rows) of ``record``; ``hidden`` is
+        bf16 or fp16 (fp16 rows are rounded to bf16 where the head reads them)."""
         ws = self._ws
-        B.clef_stream_rows(self.cfg, self.prepared.data_ptr(), schema, hidden.data_ptr(), record, row0, n_rows,
-                           ws.data_ptr(), ws.numel(), stream_handle(stream))
+        fn = B.clef_stream_rows_f16 if hidden.dtype == torch.float16 else B.clef_stream_rows
+        fn(self.cfg, self.prepared.data_ptr(), schema, hidden.data_ptr(), record, row0, n_rows, ws.data_ptr(),
+           ws.numel(), stream_handle(stream))
 
     def stream_finish(self, schema: B.Schema, hidden: torch.Tensor, token_ids: torch.Tensor, lexical: torch.Tensor,
                       out: Optional[Outputs] = None, debug=None, stream=None) -> Outputs:
         ws = self._ws
         out = out if out is not None else self.alloc_outputs(schema)
-        B.clef_stream_finish(self.cfg, self.weight_ptrs, self.prepared.data_ptr(), schema, hidden.data_ptr(),
-                             token_ids.data_ptr(), lexical.data_ptr(), out.logits.data_ptr(), out.probs.data_ptr(),
-                             out.q_value.data_ptr(), out.q_conf.data_ptr(), out.q_argmax.data_ptr(), ws.data_ptr(),
-                             ws.numel(), debug=debug, stream=stream_handle(stream))
+        fn = B.clef_stream_finish_f16 if hidden.dtype == torch.float16 else B.clef_stream_finish
+        fn(self.cfg, self.weight_ptrs, self.prepared.data_ptr(), schema, hidden.data_ptr(), token_ids.data_ptr(),
+           lexical.data_ptr(), out.logits.data_ptr(), out.probs.data_ptr(), out.q_value.data_ptr(),
+           out.q_conf.data_ptr(), out.q_argmax.data_ptr(), ws.data_ptr(), ws.numel(), debug=debug,
+           stream=stream_handle(stream))
         return out
 
     def device_status(self, stream=None) -> int:

@@ -90,3 +90,34 @@ def test_stream_irregular_chunks_any_order():
     got = _streamed(head, bt, inputs, chunks)
     for k in ref:
         np.testing.assert_array_equal(got[k], ref[k])
+
+
+def test_stream_fp16_rows_equal_rounded_bf16_and_match_oracle():
+    """fp16 hidden rows (the dtype of the CoreAI chunked readout).  The head rounds each
+    fp16 value to bf16 where it reads it, so streaming the fp16 rows must give exactly the
+    outputs of streaming the host-rounded bf16 rows; and the oracle, fed the fp16 values
+    widened exactly, must agree within the acceptance bar.  Record 0 arrives as one chunk
+    longer than the 1024-row staging pass; the others in 64-row chunks."""
+    import dataclasses
+
+    import oracle
+
+    bt = synth.make_batch(_spec(), seed=33, with_hidden=False)
+    rng = np.random.default_rng(33)
+    h16 = (rng.standard_normal((bt.B, bt.Lpad, bt.H), dtype=np.float32) * 1.5).astype(np.float16)
+    bt = dataclasses.replace(bt, hidden=synth.f32_to_bf16(h16.astype(np.float32)))
+    assert bt.lengths[0] > 1024
+    head, w = head_for(FULL)
+    hidden_b, ids, lex = device_inputs(bt, FULL.vocab)
+    hidden16 = torch.from_numpy(h16).cuda()
+    chunks = [(0, 0, int(bt.lengths[0]))]
+    chunks += [(b, r0, min(64, int(bt.lengths[b]) - r0)) for r0 in range(0, int(bt.lengths.max()), 64)
+               for b in range(1, bt.B) if r0 < bt.lengths[b]]
+    got = _streamed(head, bt, (hidden16, ids, lex), chunks)
+    ref_b = _streamed(head, bt, (hidden_b, ids, lex), chunks)
+    for k in got:
+        np.testing.assert_array_equal(got[k], ref_b[k])
+    ref = oracle.head_forward(w, FULL.heads, FULL.n_route, FULL.n_joint, lambda b: h16[b].astype(np.float64),
+                              bt.lengths, bt.q_rec, bt.q_type, bt.q_span, bt.q_opt_off, bt.o_span, bt.token_ids,
+                              bt.lexical)
+    print("fp16 stream", compare(got, ref, bt))
