@@ -154,6 +154,12 @@ typedef struct clef_debug_outputs {
     void** timeline;
     int32_t timeline_len;
     int32_t* timeline_count;
+    /* Which kernels run the per-record tail (option LayerNorm to softmax): 0 or 1, the
+     * batched chain (one GEMM per projection over the whole batch, the faster one on
+     * GB300); 2, one fused launch of a 16-CTA thread-block cluster per record group,
+     * where the head shape allows it (width 1024, 16 heads, FFN 4096, at most 256
+     * options per record).  The outputs agree within the parity tolerance either way. */
+    int32_t tail_mode;
 } clef_debug_outputs;
 
 /* The forward pass.

@@ -51,14 +51,29 @@ struct Carve {
 
 struct PreparedLayout {
     size_t wkv, ckv, bkv, wq0, wfield, total;
+    // the fused tail's sliced copies (launch_tail_slices), for the head shapes it supports
+    bool tail = false;
+    size_t t_field = 0, t_mlp1 = 0, t_qkv[kTailMaxJoint] = {}, t_o[kTailMaxJoint] = {}, t_w1[kTailMaxJoint] = {},
+           t_w2[kTailMaxJoint] = {};
     PreparedLayout(const clef_config* c) {
-        const size_t H = c->hidden, D = c->width, NKV = size_t(2) * c->n_route * D;
+        const size_t H = c->hidden, D = c->width, F = c->ffn, NKV = size_t(2) * c->n_route * D;
         Carve cv;
         wkv = cv.take(NKV * H * 2);
         ckv = cv.take(NKV * 4);
         bkv = cv.take(NKV * 4);
         wq0 = cv.take(D * 3 * H * 2);
         wfield = cv.take(D * (2 * H + D) * 2);
+        tail = record_tail_shape(c->hidden, c->width, c->heads, c->ffn, c->n_joint);
+        if (tail) {
+            t_field = cv.take(D * (2 * H + D) * 2);
+            t_mlp1 = cv.take(D * 4 * D * 2);
+            for (int i = 0; i < c->n_joint; ++i) {
+                t_qkv[i] = cv.take(3 * D * D * 2);
+                t_o[i] = cv.take(D * D * 2);
+                t_w1[i] = cv.take(F * D * 2);
+                t_w2[i] = cv.take(D * F * 2);
+            }
+        }
         total = cv.off;
     }
 };
@@ -66,11 +81,12 @@ struct PreparedLayout {
 // Host-built plan of one batch: tables the kernels index, and sizes.
 struct Plan {
     int B = 0, Q = 0, O = 0, R = 0, n_mtiles = 0, n_items = 0, n_chunks = 0, n_units = 0, max_rec_options = 0;
+    int n_groups = 0;  // record groups of the fused tail (plan_tail_groups)
     int64_t P = 0;  // attention partial rows
     std::vector<int32_t> blob;  // int32 tables followed by the int64 partial offsets
     // offsets (in int32 units) of each table in the blob
     size_t lengths, rec_row_off, rec_q_off, rec_o_off, q_rec, q_type, q_span, q_opt_off, o_rec, o_q, o_span,
-        tile_rec, tile_a_row, item, chunk_rec, chunk_idx, unit_cx, unit_qp, rec_part_off;
+        tile_rec, tile_a_row, item, chunk_rec, chunk_idx, unit_cx, unit_qp, rec_part_off, grp_rec;
 };
 
 int validate_schema(const clef_config* c, const clef_schema* s) {
@@ -246,6 +262,7 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
             }
         }
     }
+    p.grp_rec = put(B + 1);    // filled by plan_tail_groups
     if (v.size() & 1) put(1);  // 8-byte alignment of the int64 table
     p.rec_part_off = put(2 * size_t(B));
     int64_t P = 0;
@@ -256,6 +273,30 @@ void build_plan(const clef_config* c, const clef_schema* s, Plan& p) {
         P += int64_t(n) * c->heads * (ro[b + 1] - ro[b]);
     }
     p.P = P;
+}
+
+// Record groups of the fused tail: consecutive records, at most kMaxFields fields and
+// kTailMaxRecOptions options per group, and about B / clusters records per group (the
+// clusters the GPU holds at once), so that the groups run in one wave where the limits
+// allow.
+void plan_tail_groups(Plan& p, int clusters) {
+    int32_t* g = &p.blob[p.grp_rec];
+    const int per = clusters > 0 ? (p.B + clusters - 1) / clusters : 1;
+    int n = 0, cf = 0, co = 0, cr = 0;
+    g[0] = 0;
+    for (int b = 0; b < p.B; ++b) {
+        const int f = p.blob[p.rec_q_off + b + 1] - p.blob[p.rec_q_off + b];
+        const int o = p.blob[p.rec_o_off + b + 1] - p.blob[p.rec_o_off + b];
+        if (cr > 0 && (cf + f > kMaxFields || co + o > kTailMaxRecOptions || cr >= per)) {
+            g[++n] = b;
+            cf = co = cr = 0;
+        }
+        cf += f;
+        co += o;
+        ++cr;
+    }
+    g[++n] = p.B;
+    p.n_groups = n;
 }
 
 struct WsLayout {
@@ -397,6 +438,18 @@ int clef_prepare_weights(const clef_config* cfg, const void* const* weights, voi
     CK(launch_copy_cols(wf, ldf, 0, W(weights, wi.mid(4)), H, D, H, st));
     CK(launch_copy_cols(wf, ldf, H, W(weights, wi.mid(6)), H, D, H, st));
     CK(launch_copy_cols(wf, ldf, 2 * H, W(weights, wi.mid(5)), D, D, D, st));
+    if (L.tail) {  // the fused tail's weight rows, sliced per cluster CTA
+        auto dst = [&](size_t off) { return reinterpret_cast<uint16_t*>(base + off); };
+        const int F = cfg->ffn, CT = cfg->heads;  // cluster CTAs: one per head
+        CK(launch_tail_slices(wf, ldf, D / CT, 0, D, dst(L.t_field), st));
+        CK(launch_tail_slices(W(weights, wi.tail(4)), 4 * D, D / CT, 0, D, dst(L.t_mlp1), st));
+        for (int i = 0; i < cfg->n_joint; ++i) {
+            CK(launch_tail_slices(W(weights, wi.joint(i, 2)), D, 3 * D / CT, 1, D, dst(L.t_qkv[i]), st));
+            CK(launch_tail_slices(W(weights, wi.joint(i, 4)), D, D / CT, 0, D, dst(L.t_o[i]), st));
+            CK(launch_tail_slices(W(weights, wi.joint(i, 8)), D, F / CT, 0, D, dst(L.t_w1[i]), st));
+            CK(launch_tail_slices(W(weights, wi.joint(i, 10)), F, D / CT, 0, D, dst(L.t_w2[i]), st));
+        }
+    }
     return CLEF_OK;
 }
 
@@ -416,6 +469,38 @@ int clef_workspace_size(const clef_config* cfg, const clef_schema* schema, size_
 namespace {
 
 enum ForwardMode { kForwardFull = 0, kForwardAfterStream = 1 };
+
+// The per-record tail (option LayerNorm to softmax) has two implementations.  The
+// batched chain runs every projection as one GEMM over the whole batch, so each weight
+// matrix is streamed once, by up to every SM.  The fused launch (record_tail.cu) runs
+// one 16-CTA cluster per record group and saves ~30 launches, but each cluster CTA
+// streams its slice of every weight matrix itself (7.7 MB per CTA at the pages' head
+// shape), at the ~60-120 GB/s one SM takes in.  Measured on GB300 the batched chain is
+// faster for every workload tried (batch8_l16k 3.32 vs 3.52 ms per forward, the 1-record
+// reference 0.405 vs 0.417 ms), so it is the default; debug->tail_mode = 2 selects the
+// fused launch where the head shape allows it (width 1024, 16 heads, FFN 4096, at most
+// kTailMaxRecOptions options per record).
+bool use_record_tail(const clef_config* c, const Plan& p, const clef_debug_outputs* debug) {
+    if (!debug || debug->tail_mode != 2) return false;
+    if (!record_tail_shape(c->hidden, c->width, c->heads, c->ffn, c->n_joint)) return false;
+    if (p.max_rec_options > kTailMaxRecOptions) return false;
+    return record_tail_clusters() > 0;
+}
+
+// Debug copies and the launch count, after the last kernel of the forward pass.
+int finish_debug(const clef_debug_outputs* debug, int n_launch, int Q, int O, int B, int H, int D, const float* u32,
+                 const float* x32, const float* g32, const float* o_hat, const float* f_hat, cudaStream_t st) {
+    if (!debug) return CLEF_OK;
+    if (debug->timeline_count) CK(cudaMemcpyAsync(debug->timeline_count, &n_launch, 4, cudaMemcpyHostToDevice, st));
+    if (debug->pooled_u) CK(cudaMemcpyAsync(debug->pooled_u, u32, size_t(Q) * H * 4, cudaMemcpyDeviceToDevice, st));
+    if (debug->pooled_x) CK(cudaMemcpyAsync(debug->pooled_x, x32, size_t(O) * H * 4, cudaMemcpyDeviceToDevice, st));
+    if (debug->global_g) CK(cudaMemcpyAsync(debug->global_g, g32, size_t(B) * H * 4, cudaMemcpyDeviceToDevice, st));
+    if (debug->option_final)
+        CK(cudaMemcpyAsync(debug->option_final, o_hat, size_t(O) * D * 4, cudaMemcpyDeviceToDevice, st));
+    if (debug->field_final)
+        CK(cudaMemcpyAsync(debug->field_final, f_hat, size_t(Q) * D * 4, cudaMemcpyDeviceToDevice, st));
+    return CLEF_OK;
+}
 
 // The forward pass.  kForwardFull uploads the plan and computes the memory statistics
 // and K/V itself; kForwardAfterStream finds both already in the workspace (put there by
@@ -440,6 +525,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     if (v != CLEF_OK) return v;
     Plan p;
     build_plan(cfg, schema, p);
+    plan_tail_groups(p, record_tail_clusters());
     const WsLayout L(cfg, p);
     if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
 
@@ -565,6 +651,37 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.route(l, 15)); e2.out = o_res; e2.ldo = D;
         CK(dense(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, e2, flags, st)); CK(tick());
     }
+    // 6-8. the per-record tail: one cluster launch per batch when it applies (see
+    // use_record_tail), else the batched chain below
+    if (use_record_tail(cfg, p, debug)) {
+        RecordTailArgs rt{};
+        rt.B = B; rt.H = H; rt.D = D; rt.F = F; rt.n_joint = cfg->n_joint; rt.Q = Q; rt.O = O;
+        rt.n_groups = p.n_groups; rt.grp_rec = T(p.grp_rec); rt.flags = flags;
+        rt.rec_q_off = T(p.rec_q_off); rt.rec_o_off = T(p.rec_o_off); rt.q_type = T(p.q_type); rt.q_rec = T(p.q_rec);
+        rt.q_opt_off = T(p.q_opt_off); rt.o_q = T(p.o_q);
+        rt.o_res = o_res; rt.u32 = u32; rt.g32 = g32; rt.x32 = x32; rt.a_field = a_field; rt.ld_field = ld_field;
+        rt.opt_ln_w = W(weights, wi.mid(0)); rt.opt_ln_b = W(weights, wi.mid(1));
+        rt.pool_w = W(weights, wi.mid(2)); rt.pool_b = W(weights, wi.mid(3));
+        auto sl = [&](size_t off) { return reinterpret_cast<const uint16_t*>(pw + off); };
+        rt.w_field = sl(PL.t_field); rt.b_field = W(weights, wi.mid(7));
+        rt.type_emb = W(weights, wi.mid(8));
+        for (int i = 0; i < cfg->n_joint; ++i) {
+            rt.ln1_w[i] = W(weights, wi.joint(i, 0)); rt.ln1_b[i] = W(weights, wi.joint(i, 1));
+            rt.w_qkv[i] = sl(PL.t_qkv[i]); rt.b_qkv[i] = W(weights, wi.joint(i, 3));
+            rt.w_o[i] = sl(PL.t_o[i]); rt.b_o[i] = W(weights, wi.joint(i, 5));
+            rt.ln2_w[i] = W(weights, wi.joint(i, 6)); rt.ln2_b[i] = W(weights, wi.joint(i, 7));
+            rt.w_1[i] = sl(PL.t_w1[i]); rt.b_1[i] = W(weights, wi.joint(i, 9));
+            rt.w_2[i] = sl(PL.t_w2[i]); rt.b_2[i] = W(weights, wi.joint(i, 11));
+        }
+        rt.fld_ln_w = W(weights, wi.tail(0)); rt.fld_ln_b = W(weights, wi.tail(1));
+        rt.gate = W(weights, wi.tail(2)); rt.joint_scale = W(weights, wi.tail(3));
+        rt.mlp1_w = sl(PL.t_mlp1); rt.mlp1_b = W(weights, wi.tail(5));
+        rt.mlp2_w = W(weights, wi.tail(6)); rt.mlp2_b = W(weights, wi.tail(7));
+        rt.o_hat = o_hat; rt.f_hat = f_hat; rt.ln_buf = ln_buf; rt.attn_buf = attn_buf; rt.hid_buf = hid_buf; rt.z = z;
+        rt.logits = logits; rt.probs = probs; rt.q_value = q_value; rt.q_conf = q_conf; rt.q_argmax = q_argmax;
+        CK(launch_record_tail(rt, st)); CK(tick());
+        return finish_debug(debug, n_launch, Q, O, B, H, D, u32, x32, g32, o_hat, f_hat, st);
+    }
     CK(launch_layer_norm(o_res, O, D, W(weights, wi.mid(0)), W(weights, wi.mid(1)), nullptr, o_hat, st)); CK(tick());
     // 6. fields: [u | g | summary] [W_fu | W_fg | W_fs]^T + b + type embedding
     CK(launch_field_pool(o_hat, D, T(p.q_opt_off), Q, W(weights, wi.mid(2)), W(weights, wi.mid(3)), a_field, ld_field,
@@ -608,17 +725,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     sc.joint_scale = W(weights, wi.tail(3));
     sc.logits = logits; sc.probs = probs; sc.q_value = q_value; sc.q_conf = q_conf; sc.q_argmax = q_argmax;
     CK(launch_score_softmax(sc, Q, st)); CK(tick());
-    if (debug && debug->timeline_count) CK(cudaMemcpyAsync(debug->timeline_count, &n_launch, 4, cudaMemcpyHostToDevice, st));
-    if (debug) {
-        if (debug->pooled_u) CK(cudaMemcpyAsync(debug->pooled_u, u32, size_t(Q) * H * 4, cudaMemcpyDeviceToDevice, st));
-        if (debug->pooled_x) CK(cudaMemcpyAsync(debug->pooled_x, x32, size_t(O) * H * 4, cudaMemcpyDeviceToDevice, st));
-        if (debug->global_g) CK(cudaMemcpyAsync(debug->global_g, g32, size_t(B) * H * 4, cudaMemcpyDeviceToDevice, st));
-        if (debug->option_final)
-            CK(cudaMemcpyAsync(debug->option_final, o_hat, size_t(O) * D * 4, cudaMemcpyDeviceToDevice, st));
-        if (debug->field_final)
-            CK(cudaMemcpyAsync(debug->field_final, f_hat, size_t(Q) * D * 4, cudaMemcpyDeviceToDevice, st));
-    }
-    return CLEF_OK;
+    return finish_debug(debug, n_launch, Q, O, B, H, D, u32, x32, g32, o_hat, f_hat, st);
 }
 
 // Statistics and K/V of rows [row0, row0 + n_rows) of one record.  fp16 rows are first
@@ -697,6 +804,7 @@ int clef_stream_begin(const clef_config* cfg, const clef_schema* schema, void* w
     if (v != CLEF_OK) return v;
     Plan p;
     build_plan(cfg, schema, p);
+    plan_tail_groups(p, record_tail_clusters());
     const WsLayout L(cfg, p);
     if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -307,6 +307,12 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // Makes this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads through matrix descriptors).
+// Orders this thread's generic-proxy global-memory accesses before its later
+// async-proxy ones (TMA copies that read what generic stores wrote).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

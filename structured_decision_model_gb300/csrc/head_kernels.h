@@ -68,6 +68,59 @@ struct FoldArgs {
     uint16_t* out_w; float* out_c; float* out_b;
 };
 
+// The per-record tail of the head (option LayerNorm, field aggregation, the joint
+// layers, the field LayerNorm and the scorer with the softmax), one thread-block
+// cluster per record.  Weights are bf16; the joint layers' pointers are per layer.
+constexpr int kTailMaxJoint = 8;
+constexpr int kTailMaxRecOptions = 256;  // options of one record the fused tail holds at once
+
+struct RecordTailArgs {
+    int B, H, D, F, n_joint, Q, O;
+    int n_groups; const int32_t* grp_rec;   // cluster g runs records [grp_rec[g], grp_rec[g + 1])
+    int* flags;                             // device status word (bounded-wait timeouts)
+    const int32_t* rec_q_off; const int32_t* rec_o_off; const int32_t* q_type; const int32_t* q_rec;
+    const int32_t* q_opt_off; const int32_t* o_q;
+    // inputs
+    const float* o_res;                     // [O][D] option stream after routing
+    const float* u32; const float* g32; const float* x32;  // pooled vectors (fp32)
+    uint16_t* a_field; int64_t ld_field;    // [Q][2H + D] bf16: u | g (read) | summary (written)
+    // weights
+    // weights: projection matrices in the sliced layout of launch_tail_slices (each
+    // cluster CTA's rows as contiguous pre-swizzled 64-column tiles), vectors as given
+    const uint16_t* opt_ln_w; const uint16_t* opt_ln_b;
+    const uint16_t* pool_w; const uint16_t* pool_b;
+    const uint16_t* w_field; const uint16_t* b_field; const uint16_t* type_emb;  // sliced [D][2H + D], [D], [3][D]
+    const uint16_t* ln1_w[kTailMaxJoint]; const uint16_t* ln1_b[kTailMaxJoint];
+    const uint16_t* w_qkv[kTailMaxJoint]; const uint16_t* b_qkv[kTailMaxJoint];  // sliced [3D][D]
+    const uint16_t* w_o[kTailMaxJoint]; const uint16_t* b_o[kTailMaxJoint];      // sliced [D][D]
+    const uint16_t* ln2_w[kTailMaxJoint]; const uint16_t* ln2_b[kTailMaxJoint];
+    const uint16_t* w_1[kTailMaxJoint]; const uint16_t* b_1[kTailMaxJoint];      // sliced [F][D]
+    const uint16_t* w_2[kTailMaxJoint]; const uint16_t* b_2[kTailMaxJoint];      // sliced [D][F]
+    const uint16_t* fld_ln_w; const uint16_t* fld_ln_b;
+    const uint16_t* gate; const uint16_t* joint_scale;
+    const uint16_t* mlp1_w; const uint16_t* mlp1_b; const uint16_t* mlp2_w; const uint16_t* mlp2_b;  // mlp1 sliced [D][4D]
+    // scratch (workspace) and outputs
+    float* o_hat;                           // [O][D] fp32 (written)
+    float* f_hat;                           // [Q][D] fp32 (written)
+    uint16_t* ln_buf;                       // [Q][D] bf16
+    uint16_t* attn_buf;                     // [Q][D] bf16
+    uint16_t* hid_buf;                      // [Q][F] bf16
+    uint16_t* z;                            // [O][4D] bf16
+    float* logits; float* probs; float* q_value; float* q_conf; int32_t* q_argmax;
+};
+
+// Clusters of the fused tail the GPU holds at once (0: the fused tail is unavailable).
+int record_tail_clusters();
+// Whether the fused tail is built for this head shape (width 1024, 16 heads, FFN 4096).
+bool record_tail_shape(int H, int D, int heads, int F, int n_joint);
+cudaError_t launch_record_tail(const RecordTailArgs& a, cudaStream_t s);
+// The sliced weight layout of the fused tail: W [N][K] (row stride K) becomes, for each
+// of the 16 cluster CTAs r and each 64-column chunk kc, a tile of R rows x 128 bytes
+// (1024-byte aligned, 16-byte chunks in the 128-byte swizzle), tiles of one CTA
+// consecutive.  Row j of CTA r's tiles is W row r R + j (qkv = 0), or, for the fused
+// q / k / v matrix (qkv = 1, R = 3 * 64), row (j / 64) D + 64 r + j % 64.
+cudaError_t launch_tail_slices(const uint16_t* w, int K, int R, int qkv, int D, uint16_t* dst, cudaStream_t s);
+
 cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpad, int H, const int32_t* tile_rec,
                              const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,
                              cudaStream_t s);

@@ -301,3 +301,50 @@ def test_too_many_questions_is_unsupported():
     with pytest.raises(B.ClefError) as e:
         B.clef_workspace_size(cfg, schema_of(bt))
     assert e.value.status == 3
+
+
+# ------------------------------------------------------------ the two tail paths
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_tail_paths_match_oracle(mode):
+    """The per-record tail (option LayerNorm to softmax) as the batched kernel chain
+    (mode 1) and as one fused launch of a 16-CTA cluster per record (mode 2)."""
+    bt = synth.make_batch(ragged_spec(B=3), seed=41)
+    head, w = head_for(FULL)
+    bufs, dbg = _debug_buffers(bt, FULL)
+    dbg.tail_mode = mode
+    gpu = run_gpu(head, bt, debug=dbg)
+    ref = run_oracle(w, FULL, bt, keep=True)
+    o_hat = np.concatenate([ref["inter"][b]["o_hat"] for b in range(bt.B)])
+    f_hat = np.concatenate([ref["inter"][b]["f_hat"] for b in range(bt.B)])
+    assert rel_rms(bufs["option_final"].cpu().numpy(), o_hat) < 1e-2
+    assert rel_rms(bufs["field_final"].cpu().numpy(), f_hat) < 1e-2
+    print("tail mode", mode, compare(gpu, ref, bt))
+
+
+def test_fused_tail_48_fields():
+    """A record with the maximum of 48 fields (three m16 tiles of the fused tail's
+    projections) and 2-3 options per question, through the fused tail."""
+    rng = np.random.default_rng(42)
+    base = synth.make_batch(synth.BatchSpec(name="f48", B=2, lengths=[2500, 700], questions=(1, 1), options=(2, 2)),
+                            seed=42)
+    q_span, o_span, q_type, q_rec, off = [], [], [], [], [0]
+    pos = 40
+    for q in range(48):
+        n = int(rng.integers(2, 4))
+        q_span.append((pos, pos + 5)); pos += 6
+        for _ in range(n):
+            o_span.append((pos, pos + 3)); pos += 4
+        q_type.append(0 if n == 2 and q % 2 else (1 if q % 3 else 2))
+        q_rec.append(0)
+        off.append(len(o_span))
+    assert pos < 2500 and len(o_span) <= 256
+    q_span.append((100, 110)); o_span += [(200, 205), (300, 302), (400, 404)]; q_type.append(1); q_rec.append(1)
+    off.append(len(o_span))
+    bt = dataclasses.replace(base, q_rec=np.array(q_rec, np.int32), q_type=np.array(q_type, np.int32),
+                             q_span=np.array(q_span, np.int32), q_opt_off=np.array(off, np.int32),
+                             o_span=np.array(o_span, np.int32))
+    head, w = head_for(FULL)
+    dbg = B.ClefDebugOutputs()
+    dbg.tail_mode = 2
+    print("48 fields", compare(run_gpu(head, bt, debug=dbg), run_oracle(w, FULL, bt), bt))
