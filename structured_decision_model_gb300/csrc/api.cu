@@ -299,12 +299,30 @@ void plan_tail_groups(Plan& p, int clusters) {
     p.n_groups = n;
 }
 
+// Split count of a residual-stream projection of `rows` rows (its partial products are
+// summed by the LayerNorm that follows it).
+int partial_splits(int rows, int N, int K) {
+    int bn = 0, S = 1;
+    partial_split_config((rows + kTile - 1) / kTile, N, K, &bn, &S);
+    return S;
+}
+
 struct WsLayout {
     size_t flags, plan, mu, rstd, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf,
-        q_buf, attn_buf, hid_buf, o_hat, f_res, f_hat, z, pm, pl, pacc, stage, total;
+        q_buf, attn_buf, hid_buf, o_hat, f_res, f_hat, z, pm, pl, pacc, stage, part, total;
     WsLayout(const clef_config* c, const Plan& p) {
         const size_t H = c->hidden, D = c->width, F = c->ffn, NKV = size_t(2) * c->n_route * D;
         const size_t B = p.B, Q = p.Q, O = p.O, R = p.R, MQO = std::max(Q, O);
+        // split-K partial products of the residual-stream projections (option query,
+        // routing / joint output and FFN-out projections, field projection)
+        const int iD = int(D), iH = int(H), iF = int(F);
+        size_t part_elems = 0;
+        if (O > 0)
+            for (int K : {3 * iH, iD, iF})
+                part_elems = std::max(part_elems, size_t(partial_splits(int(O), iD, K)) * O * D);
+        if (Q > 0)
+            for (int K : {2 * iH + iD, iD, iF})
+                part_elems = std::max(part_elems, size_t(partial_splits(int(Q), iD, K)) * Q * D);
         Carve cv;
         flags = cv.take(256);
         plan = cv.take(p.blob.size() * 4);
@@ -329,6 +347,7 @@ struct WsLayout {
         pl = cv.take(size_t(p.P) * 4);
         pacc = cv.take(size_t(p.P) * 64 * 4);
         stage = cv.take(size_t(kStageRows) * H * 2);  // bf16 copy of fp16 streamed rows
+        part = cv.take(part_elems * 4);
         total = cv.off;
     }
 };
@@ -371,6 +390,35 @@ cudaError_t dense(const uint16_t* A, int64_t lda, int M, const uint16_t* Bw, int
     GemmEpilogue ee = e;
     ee.M = M;
     return launch_gemm(g, ee, flags, st);
+}
+
+// Residual-stream projection A [M][K] x weight [N][K]^T whose K is split over
+// independent CTAs; each split stores its fp32 partial product into its slab of `part`
+// (slab stride M * N) and the LayerNorm that follows sums them (launch_layer_norm_acc).
+cudaError_t dense_partial(const uint16_t* A, int64_t lda, int M, const uint16_t* Bw, int N, int K, float* part,
+                          int* flags, cudaStream_t st, int* splits) {
+    int bn = 0, S = 1;
+    partial_split_config((M + kTile - 1) / kTile, N, K, &bn, &S);
+    *splits = S;
+    GemmProblem g;
+    g.b_is_weight = true;
+    g.A = A;
+    g.lda = lda;
+    g.a_rows = M;
+    g.B = Bw;
+    g.ldb = K;
+    g.N = N;
+    g.K = K;
+    g.n_mtiles = (M + kTile - 1) / kTile;
+    g.defer_splits = S;
+    g.defer_bn = bn;
+    g.part_stride = int64_t(M) * N;
+    GemmEpilogue e;
+    e.kind = EPI_F32;
+    e.out = part;
+    e.ldo = N;
+    e.M = M;
+    return launch_gemm(g, e, flags, st);
 }
 
 }  // namespace
@@ -567,7 +615,19 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     float* f_res = reinterpret_cast<float*>(ws + L.f_res);
     float* f_hat = reinterpret_cast<float*>(ws + L.f_hat);
     uint16_t* z = reinterpret_cast<uint16_t*>(ws + L.z);
+    float* part = reinterpret_cast<float*>(ws + L.part);
     const int ld_field = 2 * H + D;
+    // the stream update + LayerNorm that finishes a deferred split-K projection
+    auto ln_acc = [&](float* x, int rows, int S, const uint16_t* bias, bool resid, const uint16_t* ln_w,
+                      const uint16_t* ln_b, uint16_t* out_bf16, float* out_f32, const uint16_t* table = nullptr,
+                      const int32_t* idx = nullptr) {
+        LnAccArgs la;
+        la.x = x; la.rows = rows; la.D = D; la.part = part; la.part_stride = int64_t(rows) * D; la.S = S;
+        la.bias = bias; la.row_table = table; la.row_idx = idx; la.ld_table = D; la.resid = resid ? 1 : 0;
+        la.ln_w = ln_w; la.ln_b = ln_b; la.out_bf16 = out_bf16; la.out_f32 = out_f32;
+        return launch_layer_norm_acc(la, st);
+    };
+    int splits = 1;
 
     // 1. memory row statistics (the memory LayerNorm is applied through them)
     if (mode == kForwardFull) {
@@ -593,12 +653,12 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     CK(mark(debug, 4, st));
     CK(launch_span_pool(sp, p.n_items, false, st)); CK(tick());
     CK(mark(debug, 5, st));
-    // 3. option queries: o = [c | x | u] [W_ctx | W_lex | W_qst]^T + b
-    {
-        GemmEpilogue e;
-        e.kind = EPI_F32; e.bias_bf16 = W(weights, 5); e.out = o_res; e.ldo = D;
-        CK(dense(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, e, flags, st)); CK(tick());
-    }
+    // 3. option queries: o = [c | x | u] [W_ctx | W_lex | W_qst]^T + b (the sum of the
+    // split partial products and the bias is formed by the first routing LayerNorm)
+    CK(dense_partial(a_query, 3 * H, O, reinterpret_cast<const uint16_t*>(pw + PL.wq0), D, 3 * H, part, flags, st,
+                     &splits)); CK(tick());
+    const uint16_t* pending_bias = W(weights, 5);  // bias of the projection whose partials are in `part`
+    bool pending_resid = false;
     // 4. memory K/V of every routing layer (LayerNorm folded), real rows only
     if (mode == kForwardAfterStream) {
         // K/V rows came in chunk by chunk; the round-up slack rows of each record were never
@@ -629,7 +689,8 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     ra.pm = reinterpret_cast<float*>(ws + L.pm); ra.pl = reinterpret_cast<float*>(ws + L.pl);
     ra.pacc = reinterpret_cast<float*>(ws + L.pacc); ra.out = attn_buf; ra.ldo = D;
     for (int l = 0; l < cfg->n_route; ++l) {
-        CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 0)), W(weights, wi.route(l, 1)), ln_buf, nullptr, st)); CK(tick());
+        CK(ln_acc(o_res, O, splits, pending_bias, pending_resid, W(weights, wi.route(l, 0)), W(weights, wi.route(l, 1)),
+                  ln_buf, nullptr)); CK(tick());
         GemmEpilogue eq;
         eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.route(l, 3)); eq.out = q_buf; eq.ldo = D;
         CK(dense(ln_buf, D, O, W(weights, wi.route(l, 2)), D, D, eq, flags, st)); CK(tick());
@@ -639,18 +700,19 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         CK(launch_route_attn_partial(ra, O, st)); CK(tick());
         if (l == 0) CK(mark(debug, 3, st));
         CK(launch_route_attn_merge(ra, O, st)); CK(tick());
-        GemmEpilogue eo;
-        eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.route(l, 9)); eo.out = o_res; eo.ldo = D;
-        CK(dense(attn_buf, D, O, W(weights, wi.route(l, 8)), D, D, eo, flags, st)); CK(tick());
-        CK(launch_layer_norm(o_res, O, D, W(weights, wi.route(l, 10)), W(weights, wi.route(l, 11)), ln_buf, nullptr,
-                             st)); CK(tick());
+        CK(dense_partial(attn_buf, D, O, W(weights, wi.route(l, 8)), D, D, part, flags, st, &splits)); CK(tick());
+        CK(ln_acc(o_res, O, splits, W(weights, wi.route(l, 9)), true, W(weights, wi.route(l, 10)),
+                  W(weights, wi.route(l, 11)), ln_buf, nullptr)); CK(tick());
         GemmEpilogue e1;
         e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.route(l, 13)); e1.out = hid_buf; e1.ldo = F;
         CK(dense(ln_buf, D, O, W(weights, wi.route(l, 12)), F, D, e1, flags, st)); CK(tick());
-        GemmEpilogue e2;
-        e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.route(l, 15)); e2.out = o_res; e2.ldo = D;
-        CK(dense(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, e2, flags, st)); CK(tick());
+        CK(dense_partial(hid_buf, F, O, W(weights, wi.route(l, 14)), D, F, part, flags, st, &splits)); CK(tick());
+        pending_bias = W(weights, wi.route(l, 15));
+        pending_resid = true;
     }
+    // the option stream's last projection finished, then the final option LayerNorm
+    CK(ln_acc(o_res, O, splits, pending_bias, pending_resid, W(weights, wi.mid(0)), W(weights, wi.mid(1)), nullptr,
+              o_hat)); CK(tick());
     // 6-8. the per-record tail: one cluster launch per batch when it applies (see
     // use_record_tail), else the batched chain below
     if (use_record_tail(cfg, p, debug)) {
@@ -682,35 +744,36 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         CK(launch_record_tail(rt, st)); CK(tick());
         return finish_debug(debug, n_launch, Q, O, B, H, D, u32, x32, g32, o_hat, f_hat, st);
     }
-    CK(launch_layer_norm(o_res, O, D, W(weights, wi.mid(0)), W(weights, wi.mid(1)), nullptr, o_hat, st)); CK(tick());
-    // 6. fields: [u | g | summary] [W_fu | W_fg | W_fs]^T + b + type embedding
+    // 6. fields: [u | g | summary] [W_fu | W_fg | W_fs]^T + b + type embedding (bias and
+    // type-embedding row added with the partial products by the first joint LayerNorm)
     CK(launch_field_pool(o_hat, D, T(p.q_opt_off), Q, W(weights, wi.mid(2)), W(weights, wi.mid(3)), a_field, ld_field,
                          2 * H, st)); CK(tick());
-    {
-        GemmEpilogue e;
-        e.kind = EPI_F32; e.bias_bf16 = W(weights, wi.mid(7)); e.row_table = W(weights, wi.mid(8));
-        e.row_idx = T(p.q_type); e.ld_table = D; e.out = f_res; e.ldo = D;
-        CK(dense(a_field, ld_field, Q, reinterpret_cast<const uint16_t*>(pw + PL.wfield), D, ld_field, e, flags, st)); CK(tick());
-    }
+    CK(dense_partial(a_field, ld_field, Q, reinterpret_cast<const uint16_t*>(pw + PL.wfield), D, ld_field, part, flags,
+                     st, &splits)); CK(tick());
+    pending_bias = W(weights, wi.mid(7));
+    pending_resid = false;
+    const uint16_t* pending_table = W(weights, wi.mid(8));
     // 7. joint layers over each record's fields
     for (int i = 0; i < cfg->n_joint; ++i) {
-        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 0)), W(weights, wi.joint(i, 1)), ln_buf, nullptr, st)); CK(tick());
+        CK(ln_acc(f_res, Q, splits, pending_bias, pending_resid, W(weights, wi.joint(i, 0)), W(weights, wi.joint(i, 1)),
+                  ln_buf, nullptr, pending_table, T(p.q_type))); CK(tick());
+        pending_table = nullptr;
         GemmEpilogue eq;
         eq.kind = EPI_BF16; eq.bias_bf16 = W(weights, wi.joint(i, 3)); eq.out = q_buf; eq.ldo = 3 * D;
         CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 2)), 3 * D, D, eq, flags, st)); CK(tick());
         CK(launch_field_attn(q_buf, D, cfg->heads, T(p.rec_q_off), B, 0.125f, attn_buf, st)); CK(tick());
-        GemmEpilogue eo;
-        eo.kind = EPI_F32_RESID; eo.bias_bf16 = W(weights, wi.joint(i, 5)); eo.out = f_res; eo.ldo = D;
-        CK(dense(attn_buf, D, Q, W(weights, wi.joint(i, 4)), D, D, eo, flags, st)); CK(tick());
-        CK(launch_layer_norm(f_res, Q, D, W(weights, wi.joint(i, 6)), W(weights, wi.joint(i, 7)), ln_buf, nullptr, st)); CK(tick());
+        CK(dense_partial(attn_buf, D, Q, W(weights, wi.joint(i, 4)), D, D, part, flags, st, &splits)); CK(tick());
+        CK(ln_acc(f_res, Q, splits, W(weights, wi.joint(i, 5)), true, W(weights, wi.joint(i, 6)),
+                  W(weights, wi.joint(i, 7)), ln_buf, nullptr)); CK(tick());
         GemmEpilogue e1;
         e1.kind = EPI_BF16; e1.gelu = 1; e1.bias_bf16 = W(weights, wi.joint(i, 9)); e1.out = hid_buf; e1.ldo = F;
         CK(dense(ln_buf, D, Q, W(weights, wi.joint(i, 8)), F, D, e1, flags, st)); CK(tick());
-        GemmEpilogue e2;
-        e2.kind = EPI_F32_RESID; e2.bias_bf16 = W(weights, wi.joint(i, 11)); e2.out = f_res; e2.ldo = D;
-        CK(dense(hid_buf, F, Q, W(weights, wi.joint(i, 10)), D, F, e2, flags, st)); CK(tick());
+        CK(dense_partial(hid_buf, F, Q, W(weights, wi.joint(i, 10)), D, F, part, flags, st, &splits)); CK(tick());
+        pending_bias = W(weights, wi.joint(i, 11));
+        pending_resid = true;
     }
-    CK(launch_layer_norm(f_res, Q, D, W(weights, wi.tail(0)), W(weights, wi.tail(1)), nullptr, f_hat, st)); CK(tick());
+    CK(ln_acc(f_res, Q, splits, pending_bias, pending_resid, W(weights, wi.tail(0)), W(weights, wi.tail(1)), nullptr,
+              f_hat, pending_table, T(p.q_type))); CK(tick());
     // 8. scorer MLP hidden layer, then scores, softmax and answers
     CK(launch_build_z(f_hat, o_hat, T(p.o_q), O, D, z, st)); CK(tick());
     {

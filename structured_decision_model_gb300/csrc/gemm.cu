@@ -45,6 +45,8 @@ struct GemmArgs {
     GemmEpilogue epi;
     int* dev_flags;
     int prefetch_b;                // B tiles of the first stages may be requested before the PDL wait
+    int deferred;                  // split-K without a cluster: split sp stores its raw partial
+    int64_t part_stride;           // into slab sp (elements between slabs) of the epilogue output
 };
 
 // Tile t of the persistent walk: split fastest, then N, then M.
@@ -94,7 +96,8 @@ struct GemmCfg {
 };
 
 template <int BN>
-__device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int n0, const uint32_t (&r)[16]) {
+__device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int n0, const uint32_t (&r)[16],
+                                               int64_t slab = 0) {
     float v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
@@ -130,7 +133,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int
         }
     }
     if (e.kind == EPI_F32 || e.kind == EPI_F32_RESID) {
-        float4* o = reinterpret_cast<float4*>(static_cast<float*>(e.out) + int64_t(m) * e.ldo + n0);
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(e.out) + slab + int64_t(m) * e.ldo + n0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float4 w = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t use = uint32_t(local >> 1);
             // split-K: this thread's share of the tile's bias, read while the MMAs run
             float bias_share[(BN + 127) / 128];
-            if (args.splits > 1) {
+            if (args.splits > 1 && !args.deferred) {
 #pragma unroll
                 for (int k = 0; k < (BN + 127) / 128; ++k) {
                     const int j = (threadIdx.x - 64) + 128 * k, n = id.nt * BN + j;
@@ -414,13 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int m = id.mt * BM + r_in_tile;
             const bool store = m < args.epi.M;
-            if (args.splits == 1) {
+            if (args.splits == 1 || args.deferred) {
+                const int64_t slab = args.deferred ? int64_t(id.sp) * args.part_stride : 0;
 #pragma unroll 1
                 for (int c = 0; c < BN / 16; ++c) {
                     uint32_t r[16];
                     tmem_ld16(tmem_base + uint32_t(acc * BN + c * 16) + (uint32_t(quarter * 32) << 16), r);
                     tmem_ld_wait();
-                    if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r);
+                    if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r, slab);
                 }
                 tc_fence_before();
                 if constexpr (PAIR) {
@@ -455,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    if (!PAIR && args.splits > 1) {
+    if (!PAIR && args.splits > 1 && !args.deferred) {
         // every thread of every CTA of the cluster passes both barriers, on every path
         cluster_sync();
         if (warp >= 2) {
@@ -654,7 +658,8 @@ bool launch_pair(const GemmProblem& p, const GemmArgs& a, cudaStream_t s, const 
 }
 
 template <int BN>
-cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s, int splits) {
+cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s, int splits,
+                      bool deferred = false) {
     using C = GemmCfg<BN, false>;
     const cudaError_t attr_err = kernel_attributes<BN, false>();
     if (attr_err != cudaSuccess) return attr_err;
@@ -671,11 +676,13 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     a.epi = e;
     a.dev_flags = flags;
     a.prefetch_b = p.b_is_weight ? 1 : 0;
+    a.deferred = deferred ? 1 : 0;
+    a.part_stride = p.part_stride;
     const int sms = num_sms();
     const int out_tiles = a.n_mtiles * a.n_ntiles;
     const int tiles = out_tiles * a.splits;
     if constexpr (BN == 256) {
-        if (a.splits == 1 && out_tiles > sms) {
+        if (a.splits == 1 && !deferred && out_tiles > sms) {
             a.prefetch_b = 0;
             cudaError_t err = cudaSuccess;
             if (launch_pair(p, a, s, ta, &err)) return err;
@@ -683,7 +690,7 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
         }
     }
     if (!make_tma_2d_bf16(&tb, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN)) return cudaErrorInvalidValue;
-    if (a.splits > 1)  // one CTA per (output tile, split); the splits of a tile form one cluster
+    if (a.splits > 1 && !deferred)  // one CTA per (output tile, split); the splits of a tile form one cluster
         return launch_cluster(gemm_tc_kernel<BN, false>, tiles, a.splits, C::SMEM, s, ta, tb, a);
     const int grid = tiles < sms ? tiles : sms;
     return launch_pdl(gemm_tc_kernel<BN, false>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, a);
@@ -700,9 +707,51 @@ int num_sms() {
     return n;
 }
 
+// Deferred split-K: no cluster reduction, so a split costs only its slab (written by the
+// GEMM, read back by the consumer through L2, about 8 TB/s each way), and any divisor of
+// the K blocks that leaves at least 4 blocks per split may serve.  Otherwise the same
+// estimate as the cluster splits below: operand tiles from L2 at about 11 TB/s into CTAs
+// that each take in about 90 GB/s.
+void partial_split_config(int n_mtiles, int N, int K, int* bn_out, int* splits_out) {
+    const int sms = num_sms();
+    const int kblocks = K / BK;
+    double best = 1e30;
+    int bn = 64, splits = 1;
+    for (int w : {64, 128, 256}) {
+        if (N % w) continue;
+        const int tiles = n_mtiles * (N / w);
+        for (int S = 1; S <= kblocks; ++S) {
+            if (kblocks % S || (S > 1 && kblocks / S < 4) || tiles * S > 2 * sms) continue;
+            const int ctas = std::min(tiles * S, sms);
+            const int waves = (tiles * S + sms - 1) / sms;
+            const double per_cta = double(waves) * (kblocks / S) * (BM + w) * BK * 2.0;
+            const double slabs = 2.0 * S * n_mtiles * double(BM) * N * 4.0;
+            const double t = std::max(per_cta / 90e3, per_cta * ctas / 11e6) + slabs / 8e6;
+            if (t < best) {
+                best = t;
+                bn = w;
+                splits = S;
+            }
+        }
+    }
+    *bn_out = bn;
+    *splits_out = splits;
+}
+
 cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_flags, cudaStream_t s, int force_bn) {
     if (p.n_mtiles <= 0 || p.N <= 0) return cudaSuccess;
     if (p.K % BK != 0 || p.N % 64 != 0 || p.lda % 8 != 0 || p.ldb % 8 != 0) return cudaErrorInvalidValue;
+    if (p.defer_splits > 0) {
+        if (e.kind != EPI_F32 || e.gelu || e.bias_bf16 || e.bias_f32 || e.row_table || (p.K / BK) % p.defer_splits ||
+            p.N % p.defer_bn)
+            return cudaErrorInvalidValue;
+        switch (p.defer_bn) {
+            case 256: return launch_bn<256>(p, e, dev_flags, s, p.defer_splits, true);
+            case 128: return launch_bn<128>(p, e, dev_flags, s, p.defer_splits, true);
+            case 64: return launch_bn<64>(p, e, dev_flags, s, p.defer_splits, true);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     const int sms = num_sms();
     const int kblocks = p.K / BK;
     int bn = force_bn, splits = 1;

@@ -262,75 +262,150 @@ __global__ void __launch_bounds__(256, 3) span_pool_kernel(SpanPoolArgs a) {
 }
 
 // =====================================================================
-// LayerNorm of fp32 rows of width D (pre-LN of the routing / joint layers and the
-// final option / field norms).  Two-pass statistics over the row held in registers.
+// A residual-stream projection finished and normalised in one pass: the projection's
+// split-K partial products (S fp32 slabs from the tensor-core GEMM) are summed, then
+// its bias, the type-embedding row (field projection) and the stream's previous value
+// (residual projections) are added, the stream is updated, and the LayerNorm that
+// follows the projection in the layer is applied (pre-LN of the next sub-layer, or the
+// final option / field norm).
+// One CTA of kAccGroups x 128 threads per row.  Group g sums slabs g, g + G, g + 2G, ...
+// in that order (G = min(S, kAccGroups) groups, so that G slab loads are in flight per
+// chunk); the group sums are then added in group order, so the result does not depend
+// on timing.  Thread t of group 0 owns the 8-column chunks t, t + 128, ... for the rest.
 // =====================================================================
-// One warp per row; lane l owns the 8-column chunks l, l + 32, ... (NCK of them at
-// most), so the row, the weight and the bias are all loaded with 16-byte accesses in
-// one round trip before the two reductions.
+constexpr int kAccGroups = 2;
+
 template <int NCK>
-__global__ void __launch_bounds__(256) layer_norm_kernel(const float* __restrict__ x, int rows, int D,
-                                                        const uint16_t* __restrict__ w,
-                                                        const uint16_t* __restrict__ bias,
-                                                        uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32) {
+__global__ void __launch_bounds__(128 * kAccGroups) layer_norm_acc_kernel(const LnAccArgs a) {
     griddep_wait();
     griddep_launch();
+    __shared__ float4 xch[kAccGroups - 1][NCK][128][2];
+    __shared__ float red[2][kAccGroups * 4];
+    const int r = blockIdx.x, t = threadIdx.x & 127, grp = threadIdx.x >> 7;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 8 + warp;
-    if (r >= rows) return;
-    const int nc = D >> 3;  // 8-column chunks in the row
-    const float4* row = reinterpret_cast<const float4*>(x + int64_t(r) * D);
+    const int D = a.D, nc = D >> 3;
+    const int G = min(a.S, kAccGroups);
     float v[NCK][8];
-    uint4 wv[NCK], bv[NCK];
-    float s = 0.f;
 #pragma unroll
-    for (int k = 0; k < NCK; ++k) {
-        const int c = lane + 32 * k;
-        if (c < nc) {
-            const float4 a0 = row[2 * c], a1 = row[2 * c + 1];
-            wv[k] = __ldg(reinterpret_cast<const uint4*>(w) + c);
-            bv[k] = __ldg(reinterpret_cast<const uint4*>(bias) + c);
-            v[k][0] = a0.x; v[k][1] = a0.y; v[k][2] = a0.z; v[k][3] = a0.w;
-            v[k][4] = a1.x; v[k][5] = a1.y; v[k][6] = a1.z; v[k][7] = a1.w;
+    for (int k = 0; k < NCK; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[k][j] = 0.f;
+    // group 0 requests everything else the row needs together with its slabs: bias,
+    // type-embedding row, previous stream value and the LayerNorm affine
+    uint4 bias_v[NCK], tab_v[NCK], lnw_v[NCK], lnb_v[NCK];
+    float4 x_v[NCK][2];
+    if (grp == 0) {
+        const uint16_t* trow = a.row_table ? a.row_table + int64_t(a.row_idx[r]) * a.ld_table : nullptr;
+#pragma unroll
+        for (int k = 0; k < NCK; ++k) {
+            const int c = t + 128 * k;
+            if (c >= nc) continue;
+            bias_v[k] = a.bias ? __ldg(reinterpret_cast<const uint4*>(a.bias) + c) : make_uint4(0, 0, 0, 0);
+            tab_v[k] = trow ? __ldg(reinterpret_cast<const uint4*>(trow) + c) : make_uint4(0, 0, 0, 0);
+            lnw_v[k] = __ldg(reinterpret_cast<const uint4*>(a.ln_w) + c);
+            lnb_v[k] = __ldg(reinterpret_cast<const uint4*>(a.ln_b) + c);
+            const float4* xr = reinterpret_cast<const float4*>(a.x + int64_t(r) * D) + 2 * c;
+            x_v[k][0] = a.resid ? xr[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+            x_v[k][1] = a.resid ? xr[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    if (grp < G) {
+#pragma unroll
+        for (int k = 0; k < NCK; ++k) {
+            const int c = t + 128 * k;
+            if (c >= nc) continue;
+            const float* pr = a.part + int64_t(r) * D + 8 * c;
+#pragma unroll 4
+            for (int sp = grp; sp < a.S; sp += G) {
+                const float4 p0 = reinterpret_cast<const float4*>(pr + sp * a.part_stride)[0];
+                const float4 p1 = reinterpret_cast<const float4*>(pr + sp * a.part_stride)[1];
+                v[k][0] += p0.x; v[k][1] += p0.y; v[k][2] += p0.z; v[k][3] += p0.w;
+                v[k][4] += p1.x; v[k][5] += p1.y; v[k][6] += p1.z; v[k][7] += p1.w;
+            }
+            if (grp > 0) {
+                xch[grp - 1][k][t][0] = make_float4(v[k][0], v[k][1], v[k][2], v[k][3]);
+                xch[grp - 1][k][t][1] = make_float4(v[k][4], v[k][5], v[k][6], v[k][7]);
+            }
+        }
+    }
+    __syncthreads();
+    float s = 0.f;
+    if (grp == 0) {
+#pragma unroll
+        for (int k = 0; k < NCK; ++k) {
+            const int c = t + 128 * k;
+            if (c >= nc) continue;
+            for (int g = 1; g < G; ++g) {
+                const float4 p0 = xch[g - 1][k][t][0], p1 = xch[g - 1][k][t][1];
+                v[k][0] += p0.x; v[k][1] += p0.y; v[k][2] += p0.z; v[k][3] += p0.w;
+                v[k][4] += p1.x; v[k][5] += p1.y; v[k][6] += p1.z; v[k][7] += p1.w;
+            }
+            if (a.bias) {
+                const uint4 b = bias_v[k];
+                v[k][0] += bf16_lo(b.x); v[k][1] += bf16_hi(b.x); v[k][2] += bf16_lo(b.y); v[k][3] += bf16_hi(b.y);
+                v[k][4] += bf16_lo(b.z); v[k][5] += bf16_hi(b.z); v[k][6] += bf16_lo(b.w); v[k][7] += bf16_hi(b.w);
+            }
+            if (a.row_table) {
+                const uint4 b = tab_v[k];
+                v[k][0] += bf16_lo(b.x); v[k][1] += bf16_hi(b.x); v[k][2] += bf16_lo(b.y); v[k][3] += bf16_hi(b.y);
+                v[k][4] += bf16_lo(b.z); v[k][5] += bf16_hi(b.z); v[k][6] += bf16_lo(b.w); v[k][7] += bf16_hi(b.w);
+            }
+            float4* xr = reinterpret_cast<float4*>(a.x + int64_t(r) * D) + 2 * c;
+            if (a.resid) {
+                const float4 o0 = x_v[k][0], o1 = x_v[k][1];
+                v[k][0] += o0.x; v[k][1] += o0.y; v[k][2] += o0.z; v[k][3] += o0.w;
+                v[k][4] += o1.x; v[k][5] += o1.y; v[k][6] += o1.z; v[k][7] += o1.w;
+            }
+            xr[0] = make_float4(v[k][0], v[k][1], v[k][2], v[k][3]);
+            xr[1] = make_float4(v[k][4], v[k][5], v[k][6], v[k][7]);
 #pragma unroll
             for (int j = 0; j < 8; ++j) s += v[k][j];
         }
     }
-    const float m = warp_sum(s) / float(D);
+    s = warp_sum(s);
+    if (lane == 0) red[0][warp] = s;
+    __syncthreads();
+    const float m = (red[0][0] + red[0][1] + red[0][2] + red[0][3]) / float(D);
     float q = 0.f;
+    if (grp == 0) {
 #pragma unroll
-    for (int k = 0; k < NCK; ++k) {
-        if (lane + 32 * k < nc) {
+        for (int k = 0; k < NCK; ++k) {
+            if (t + 128 * k < nc) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float d = v[k][j] - m;
-                q += d * d;
+                for (int j = 0; j < 8; ++j) {
+                    const float d = v[k][j] - m;
+                    q += d * d;
+                }
             }
         }
     }
-    const float rs = rsqrtf(warp_sum(q) / float(D) + 1e-5f);
+    q = warp_sum(q);
+    if (lane == 0) red[1][warp] = q;
+    __syncthreads();
+    if (grp != 0) return;
+    const float rs = rsqrtf((red[1][0] + red[1][1] + red[1][2] + red[1][3]) / float(D) + 1e-5f);
 #pragma unroll
     for (int k = 0; k < NCK; ++k) {
-        const int c = lane + 32 * k;
-        if (c < nc) {
-            const float gm[8] = {bf16_lo(wv[k].x), bf16_hi(wv[k].x), bf16_lo(wv[k].y), bf16_hi(wv[k].y),
-                                 bf16_lo(wv[k].z), bf16_hi(wv[k].z), bf16_lo(wv[k].w), bf16_hi(wv[k].w)};
-            const float bt[8] = {bf16_lo(bv[k].x), bf16_hi(bv[k].x), bf16_lo(bv[k].y), bf16_hi(bv[k].y),
-                                 bf16_lo(bv[k].z), bf16_hi(bv[k].z), bf16_lo(bv[k].w), bf16_hi(bv[k].w)};
-            float y[8];
+        const int c = t + 128 * k;
+        if (c >= nc) continue;
+        const uint4 wv = lnw_v[k], bv = lnb_v[k];
+        const float gm[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                             bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+        const float bt[8] = {bf16_lo(bv.x), bf16_hi(bv.x), bf16_lo(bv.y), bf16_hi(bv.y),
+                             bf16_lo(bv.z), bf16_hi(bv.z), bf16_lo(bv.w), bf16_hi(bv.w)};
+        float y[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) y[j] = (v[k][j] - m) * rs * gm[j] + bt[j];
-            if (out_bf16) {
-                uint4 o;
-                o.x = pack_bf16(y[0], y[1]); o.y = pack_bf16(y[2], y[3]);
-                o.z = pack_bf16(y[4], y[5]); o.w = pack_bf16(y[6], y[7]);
-                reinterpret_cast<uint4*>(out_bf16 + int64_t(r) * D)[c] = o;
-            }
-            if (out_f32) {
-                float4* o = reinterpret_cast<float4*>(out_f32 + int64_t(r) * D);
-                o[2 * c] = make_float4(y[0], y[1], y[2], y[3]);
-                o[2 * c + 1] = make_float4(y[4], y[5], y[6], y[7]);
-            }
+        for (int j = 0; j < 8; ++j) y[j] = (v[k][j] - m) * rs * gm[j] + bt[j];
+        if (a.out_bf16) {
+            uint4 o;
+            o.x = pack_bf16(y[0], y[1]); o.y = pack_bf16(y[2], y[3]);
+            o.z = pack_bf16(y[4], y[5]); o.w = pack_bf16(y[6], y[7]);
+            reinterpret_cast<uint4*>(a.out_bf16 + int64_t(r) * D)[c] = o;
+        }
+        if (a.out_f32) {
+            float4* o = reinterpret_cast<float4*>(a.out_f32 + int64_t(r) * D);
+            o[2 * c] = make_float4(y[0], y[1], y[2], y[3]);
+            o[2 * c + 1] = make_float4(y[4], y[5], y[6], y[7]);
         }
     }
 }
@@ -707,15 +782,12 @@ cudaError_t launch_f16_rows_to_bf16(const uint16_t* src, int64_t ld_src, int row
                       H, dst);
 }
 
-cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
-                              uint16_t* out_bf16, float* out_f32, cudaStream_t s) {
-    if (rows <= 0) return cudaSuccess;
-    const dim3 grid((rows + 7) / 8);
-    if (D % 8 != 0 || D > 2048) return cudaErrorInvalidValue;
-    if (D <= 256) return launch_pdl(layer_norm_kernel<1>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
-    if (D <= 512) return launch_pdl(layer_norm_kernel<2>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
-    if (D <= 1024) return launch_pdl(layer_norm_kernel<4>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
-    return launch_pdl(layer_norm_kernel<8>, grid, dim3(256), 0, s, x, rows, D, w, b, out_bf16, out_f32);
+cudaError_t launch_layer_norm_acc(const LnAccArgs& a, cudaStream_t s) {
+    if (a.rows <= 0) return cudaSuccess;
+    if (a.D % 8 != 0 || a.D > 2048 || a.S < 1 || !a.part || !a.x || !a.ln_w || !a.ln_b) return cudaErrorInvalidValue;
+    const dim3 block(128 * kAccGroups);
+    if (a.D <= 1024) return launch_pdl(layer_norm_acc_kernel<1>, dim3(unsigned(a.rows)), block, 0, s, a);
+    return launch_pdl(layer_norm_acc_kernel<2>, dim3(unsigned(a.rows)), block, 0, s, a);
 }
 
 cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_off, int Q, const uint16_t* w_a,

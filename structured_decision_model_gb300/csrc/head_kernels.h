@@ -132,8 +132,26 @@ cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off
 cudaError_t launch_span_pool(const SpanPoolArgs& a, int n_items, bool raw, cudaStream_t s);
 cudaError_t launch_f16_rows_to_bf16(const uint16_t* src, int64_t ld_src, int rows, int H, uint16_t* dst,
                                     cudaStream_t s);
-cudaError_t launch_layer_norm(const float* x, int rows, int D, const uint16_t* w, const uint16_t* b,
-                              uint16_t* out_bf16, float* out_f32, cudaStream_t s);
+// A residual-stream projection finished from its deferred split-K partial products,
+// followed by a LayerNorm: x = sum_s part[s] + bias + row_table[row_idx] (+ x when
+// resid), the stream x updated, then LN(x) with (ln_w, ln_b) into out_bf16 / out_f32.
+struct LnAccArgs {
+    float* x = nullptr;                   // [rows][D] fp32 stream (read when resid, always written)
+    int rows = 0, D = 0;
+    const float* part = nullptr;          // S slabs [rows][D], slab stride part_stride elements
+    int64_t part_stride = 0;
+    int S = 0;
+    const uint16_t* bias = nullptr;       // [D] bf16 or null
+    const uint16_t* row_table = nullptr;  // [*][ld_table] bf16 rows added by row_idx[r], or null
+    const int32_t* row_idx = nullptr;
+    int64_t ld_table = 0;
+    int resid = 0;
+    const uint16_t* ln_w = nullptr;
+    const uint16_t* ln_b = nullptr;
+    uint16_t* out_bf16 = nullptr;         // [rows][D] or null
+    float* out_f32 = nullptr;             // [rows][D] or null
+};
+cudaError_t launch_layer_norm_acc(const LnAccArgs& a, cudaStream_t s);
 cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int O,
                                       cudaStream_t s);
 cudaError_t launch_route_attn_merge(const RouteAttnArgs& a, int O, cudaStream_t s);

@@ -76,9 +76,20 @@ struct GemmProblem {
     // B is never written by a kernel that may still be running on the stream (weights): its
     // first tiles may then be requested before waiting for the previous kernel of the stream
     bool b_is_weight = false;
+    // deferred split-K (defer_splits > 0, widths from partial_split_config): defer_splits
+    // CTAs per output tile of width defer_bn, each storing its raw fp32 partial product into
+    // slab sp of the epilogue output (slab stride part_stride elements; the epilogue must be
+    // a plain EPI_F32 store); the consumer sums the slabs in split order
+    int defer_splits = 0;
+    int defer_bn = 0;
+    int64_t part_stride = 0;
 };
 
 int num_sms();
+
+// Tile width and split count of a deferred split-K product: a function of the
+// output-tile count, N and K only.
+void partial_split_config(int n_mtiles, int N, int K, int* bn, int* splits);
 
 // 2-D TMA descriptor of a row-major bf16 matrix [rows][inner] (row stride in elements),
 // 64-element x box_rows box, 128-byte swizzle.  Returns false if the driver rejects it.
