@@ -772,10 +772,17 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         pending_bias = W(weights, wi.joint(i, 11));
         pending_resid = true;
     }
-    CK(ln_acc(f_res, Q, splits, pending_bias, pending_resid, W(weights, wi.tail(0)), W(weights, wi.tail(1)), nullptr,
-              f_hat, pending_table, T(p.q_type))); CK(tick());
+    // the field stream's last projection finished, the final field LayerNorm, and the scorer
+    // MLP input z_j = [f_hat_q, o_hat_j, f_hat_q * o_hat_j, |f_hat_q - o_hat_j|] of each option
+    {
+        LnAccArgs la;
+        la.x = f_res; la.rows = Q; la.D = D; la.part = part; la.part_stride = int64_t(Q) * D; la.S = splits;
+        la.bias = pending_bias; la.row_table = pending_table; la.row_idx = T(p.q_type); la.ld_table = D;
+        la.resid = pending_resid ? 1 : 0; la.ln_w = W(weights, wi.tail(0)); la.ln_b = W(weights, wi.tail(1));
+        la.out_f32 = f_hat; la.z = z; la.z_opt_off = T(p.q_opt_off); la.z_o_hat = o_hat;
+        CK(launch_layer_norm_acc(la, st)); CK(tick());
+    }
     // 8. scorer MLP hidden layer, then scores, softmax and answers
-    CK(launch_build_z(f_hat, o_hat, T(p.o_q), O, D, z, st)); CK(tick());
     {
         GemmEpilogue e;
         e.kind = EPI_BF16; e.gelu = 1; e.bias_bf16 = W(weights, wi.tail(5)); e.out = hid_buf; e.ldo = D;

@@ -122,27 +122,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += e.bias_f32[n0 + j];
         }
-        if (e.row_table) {
-            const uint16_t* t = e.row_table + int64_t(e.row_idx[m]) * e.ld_table;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += bf16_to_float(t[n0 + j]);
-        }
         if (e.gelu) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = gelu_exact(v[j]);
         }
     }
-    if (e.kind == EPI_F32 || e.kind == EPI_F32_RESID) {
+    if (e.kind == EPI_F32) {
         float4* o = reinterpret_cast<float4*>(static_cast<float*>(e.out) + slab + int64_t(m) * e.ldo + n0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float4 w = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            if (e.kind == EPI_F32_RESID) {
-                float4 old = o[q];
-                w.x += old.x; w.y += old.y; w.z += old.z; w.w += old.w;
-            }
-            o[q] = w;
-        }
+        for (int q = 0; q < 4; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     } else {
         uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.out) + int64_t(m) * e.ldo + n0);
 #pragma unroll
@@ -158,32 +146,20 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int
 }
 
 // The split-K reduction's epilogue (never the LN fold): columns n0 .. n0 + 15 of row m,
-// the bias read from the tile's staged copy `sbias` (column n0 at sbias[0]) and, for
-// EPI_F32_RESID, the residual chunk already loaded into `res`.
+// the bias read from the tile's staged copy `sbias` (column n0 at sbias[0]).
 __device__ __forceinline__ void epilogue_chunk_split(const GemmEpilogue& e, int m, int n0, const float* sbias,
-                                                     const float (&acc)[16], const float4 (&res)[4]) {
+                                                     const float (&acc)[16]) {
     float v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = acc[j] + sbias[j];
-    if (e.row_table) {
-        const uint16_t* t = e.row_table + int64_t(e.row_idx[m]) * e.ld_table;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] += bf16_to_float(t[n0 + j]);
-    }
     if (e.gelu) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = gelu_exact(v[j]);
     }
-    if (e.kind == EPI_F32 || e.kind == EPI_F32_RESID) {
+    if (e.kind == EPI_F32) {
         float4* o = reinterpret_cast<float4*>(static_cast<float*>(e.out) + int64_t(m) * e.ldo + n0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float4 w = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            if (e.kind == EPI_F32_RESID) {
-                w.x += res[q].x; w.y += res[q].y; w.z += res[q].z; w.w += res[q].w;
-            }
-            o[q] = w;
-        }
+        for (int q = 0; q < 4; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     } else {
         uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.out) + int64_t(m) * e.ldo + n0);
 #pragma unroll
@@ -474,13 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t off = red0 + uint32_t((row * kRedLd + c * 16) * 4);
                 const int m = id.mt * BM + row;
                 const int n0 = id.nt * BN + c * 16;
-                float4 res[4];
-                if (args.epi.kind == EPI_F32_RESID && m < args.epi.M) {  // read ahead of the partial sums
-                    const float4* o = reinterpret_cast<const float4*>(static_cast<const float*>(args.epi.out) +
-                                                                      int64_t(m) * args.epi.ldo + n0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) res[q] = o[q];
-                }
                 // every split's slice is requested before any is added (one round trip),
                 // then the slices are summed in split order
                 float4 w[kMaxSplits][4];
@@ -505,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (m < args.epi.M) epilogue_chunk_split(args.epi, m, n0, sbias + c * 16, v, res);
+                if (m < args.epi.M) epilogue_chunk_split(args.epi, m, n0, sbias + c * 16, v);
             }
         }
         cluster_sync();  // no CTA leaves while another may still read its shared memory
@@ -742,7 +711,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_fl
     if (p.n_mtiles <= 0 || p.N <= 0) return cudaSuccess;
     if (p.K % BK != 0 || p.N % 64 != 0 || p.lda % 8 != 0 || p.ldb % 8 != 0) return cudaErrorInvalidValue;
     if (p.defer_splits > 0) {
-        if (e.kind != EPI_F32 || e.gelu || e.bias_bf16 || e.bias_f32 || e.row_table || (p.K / BK) % p.defer_splits ||
+        if (e.kind != EPI_F32 || e.gelu || e.bias_bf16 || e.bias_f32 || (p.K / BK) % p.defer_splits ||
             p.N % p.defer_bn)
             return cudaErrorInvalidValue;
         switch (p.defer_bn) {

@@ -407,6 +407,41 @@ __global__ void __launch_bounds__(128 * kAccGroups) layer_norm_acc_kernel(const 
             o[2 * c] = make_float4(y[0], y[1], y[2], y[3]);
             o[2 * c + 1] = make_float4(y[4], y[5], y[6], y[7]);
         }
+        if (a.z) {  // the scorer MLP input of every option of this row's question
+            const int j0 = a.z_opt_off[r], j1 = a.z_opt_off[r + 1];
+            for (int jb = j0; jb < j1; jb += 4) {
+                float4 ov[4][2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)  // four options' chunks requested before any is used
+                    if (jb + u < j1) {
+                        const float4* op = reinterpret_cast<const float4*>(a.z_o_hat + int64_t(jb + u) * D) + 2 * c;
+                        ov[u][0] = op[0];
+                        ov[u][1] = op[1];
+                    }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (jb + u >= j1) break;
+                    const float o[8] = {ov[u][0].x, ov[u][0].y, ov[u][0].z, ov[u][0].w,
+                                        ov[u][1].x, ov[u][1].y, ov[u][1].z, ov[u][1].w};
+                    uint4 pf, po, pm, pd;
+                    pf.x = pack_bf16(y[0], y[1]); pf.y = pack_bf16(y[2], y[3]);
+                    pf.z = pack_bf16(y[4], y[5]); pf.w = pack_bf16(y[6], y[7]);
+                    po.x = pack_bf16(o[0], o[1]); po.y = pack_bf16(o[2], o[3]);
+                    po.z = pack_bf16(o[4], o[5]); po.w = pack_bf16(o[6], o[7]);
+                    pm.x = pack_bf16(y[0] * o[0], y[1] * o[1]); pm.y = pack_bf16(y[2] * o[2], y[3] * o[3]);
+                    pm.z = pack_bf16(y[4] * o[4], y[5] * o[5]); pm.w = pack_bf16(y[6] * o[6], y[7] * o[7]);
+                    pd.x = pack_bf16(fabsf(y[0] - o[0]), fabsf(y[1] - o[1]));
+                    pd.y = pack_bf16(fabsf(y[2] - o[2]), fabsf(y[3] - o[3]));
+                    pd.z = pack_bf16(fabsf(y[4] - o[4]), fabsf(y[5] - o[5]));
+                    pd.w = pack_bf16(fabsf(y[6] - o[6]), fabsf(y[7] - o[7]));
+                    uint4* zr = reinterpret_cast<uint4*>(a.z + int64_t(jb + u) * 4 * D);
+                    zr[c] = pf;
+                    zr[(D >> 3) + c] = po;
+                    zr[2 * (D >> 3) + c] = pm;
+                    zr[3 * (D >> 3) + c] = pd;
+                }
+            }
+        }
     }
 }
 
@@ -527,26 +562,6 @@ __global__ void __launch_bounds__(128) field_attn_kernel(const uint16_t* __restr
         w.z = pack_bf16(o[4], o[5]); w.w = pack_bf16(o[6], o[7]);
         *reinterpret_cast<uint4*>(out + int64_t(q0 + r) * D + h * 64 + c8) = w;
     }
-}
-
-// =====================================================================
-// Scorer MLP input ("clef-4bit JointSchemaHead walkthrough" section 3 step 4):
-// z_j = [f_hat_q, o_hat_j, f_hat_q * o_hat_j, |f_hat_q - o_hat_j|], bf16 [O][4D].
-// =====================================================================
-__global__ void __launch_bounds__(256) build_z_kernel(const float* __restrict__ f_hat, const float* __restrict__ o_hat,
-                                                     const int32_t* __restrict__ o_q, int O, int D,
-                                                     uint16_t* __restrict__ z) {
-    griddep_wait();
-    griddep_launch();
-    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= int64_t(O) * D) return;
-    const int j = int(i / D), c = int(i % D);
-    const float f = f_hat[int64_t(o_q[j]) * D + c], o = o_hat[i];
-    uint16_t* row = z + int64_t(j) * 4 * D;
-    row[c] = float_to_bf16(f);
-    row[D + c] = float_to_bf16(o);
-    row[2 * D + c] = float_to_bf16(f * o);
-    row[3 * D + c] = float_to_bf16(fabsf(f - o));
 }
 
 // =====================================================================
@@ -800,13 +815,6 @@ cudaError_t launch_field_attn(const uint16_t* qkv, int D, int heads, const int32
                               uint16_t* out, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     return launch_pdl(field_attn_kernel, dim3(B, heads), dim3(128), 0, s, qkv, D, rec_q_off, scale, out);
-}
-
-cudaError_t launch_build_z(const float* f_hat, const float* o_hat, const int32_t* o_q, int O, int D, uint16_t* z,
-                           cudaStream_t s) {
-    const int64_t n = int64_t(O) * D;
-    if (n <= 0) return cudaSuccess;
-    return launch_pdl(build_z_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, s, f_hat, o_hat, o_q, O, D, z);
 }
 
 cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s) {

@@ -150,6 +150,11 @@ struct LnAccArgs {
     const uint16_t* ln_b = nullptr;
     uint16_t* out_bf16 = nullptr;         // [rows][D] or null
     float* out_f32 = nullptr;             // [rows][D] or null
+    // scorer MLP input rows z_j = [y_q, o_hat_j, y_q * o_hat_j, |y_q - o_hat_j|] (bf16
+    // [O][4D]) for the options j of row q (z_opt_off[q] .. z_opt_off[q + 1]), or null
+    uint16_t* z = nullptr;
+    const int32_t* z_opt_off = nullptr;
+    const float* z_o_hat = nullptr;       // [O][D]
 };
 cudaError_t launch_layer_norm_acc(const LnAccArgs& a, cudaStream_t s);
 cudaError_t launch_route_attn_partial(const RouteAttnArgs& a, int O,
@@ -159,8 +164,6 @@ cudaError_t launch_field_pool(const float* o_hat, int D, const int32_t* q_opt_of
                               const uint16_t* b_a, uint16_t* out, int64_t ldo, int col_off, cudaStream_t s);
 cudaError_t launch_field_attn(const uint16_t* qkv, int D, int heads, const int32_t* rec_q_off, int B, float scale,
                               uint16_t* out, cudaStream_t s);
-cudaError_t launch_build_z(const float* f_hat, const float* o_hat, const int32_t* o_q, int O, int D, uint16_t* z,
-                           cudaStream_t s);
 cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s);
 cudaError_t launch_fold_kv(const FoldArgs& a, int rows, cudaStream_t s);
 cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaStream_t s);

@@ -39,8 +39,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // ------------------------------------------------------------------ the GEMM
 
 enum EpiKind : int {
-    EPI_F32 = 0,        // out_f32 = acc + bias (+ table[row_idx[m]])
-    EPI_F32_RESID = 1,  // out_f32 += acc + bias  (residual stream update)
+    EPI_F32 = 0,        // out_f32 = acc + bias
     EPI_BF16 = 2,       // out_bf16 = act(acc + bias)
     EPI_KV_LNFOLD = 3,  // out_bf16 = rstd[m] * (acc - mu[m] * col_c[n]) + bias_f32[n]
 };
@@ -53,9 +52,6 @@ struct GemmEpilogue {
     const float* row_mu = nullptr;        // [rows] (LN fold)
     const float* row_rstd = nullptr;      // [rows] (LN fold)
     const float* col_c = nullptr;         // [N]    (LN fold)
-    const uint16_t* row_table = nullptr;  // [*, N] bf16 rows added by index (type embedding)
-    const int32_t* row_idx = nullptr;     // [rows]
-    int64_t ld_table = 0;
     void* out = nullptr;
     int64_t ldo = 0;
     int M = 0;  // rows that are stored (m < M)
