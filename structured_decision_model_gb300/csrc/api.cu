@@ -310,6 +310,7 @@ int partial_splits(int rows, int N, int K) {
 struct WsLayout {
     size_t flags, plan, mu, rstd, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf,
         q_buf, attn_buf, hid_buf, o_hat, f_res, f_hat, z, pm, pl, pacc, stage, part, total;
+    WsLayout() = default;
     WsLayout(const clef_config* c, const Plan& p) {
         const size_t H = c->hidden, D = c->width, F = c->ffn, NKV = size_t(2) * c->n_route * D;
         const size_t B = p.B, Q = p.Q, O = p.O, R = p.R, MQO = std::max(Q, O);
@@ -351,6 +352,71 @@ struct WsLayout {
         total = cv.off;
     }
 };
+
+// The validated plan and workspace layout of the schema this thread passed last.  The
+// calls of one batch (workspace size, stream begin, every chunk, stream finish, forward)
+// pass the same tables again and again, so each call compares them, element by element,
+// with the copy kept from the previous call and validates and rebuilds only when they
+// differ (or the configuration or the current device does).
+struct PlanCache {
+    bool valid = false;
+    clef_config cfg{};
+    int device = -1;
+    int32_t B = 0, Lpad = 0, Q = 0, O = 0;
+    int64_t row_stride = 0;
+    std::vector<int32_t> tables;  // lengths | q_rec | q_type | q_span | q_opt_off | o_span
+    Plan plan;
+    WsLayout layout;
+};
+
+int cached_plan(const clef_config* cfg, const clef_schema* s, const Plan** plan, const WsLayout** layout) {
+    thread_local PlanCache c;
+    if (!s || !s->lengths || !s->q_rec || !s->q_type || !s->q_span || !s->q_opt_off || !s->o_span || s->B < 1 ||
+        s->Q < 1 || s->O < 1)
+        return CLEF_ERR_INVALID_ARGUMENT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        dev = -1;
+    }
+    const size_t nB = size_t(s->B), nQ = size_t(s->Q), nO = size_t(s->O);
+    const std::pair<const int32_t*, size_t> parts[] = {{s->lengths, nB},     {s->q_rec, nQ},       {s->q_type, nQ},
+                                                       {s->q_span, 2 * nQ},  {s->q_opt_off, nQ + 1}, {s->o_span, 2 * nO}};
+    bool hit = c.valid && std::memcmp(&c.cfg, cfg, sizeof(clef_config)) == 0 && c.device == dev && c.B == s->B &&
+               c.Lpad == s->Lpad && c.Q == s->Q && c.O == s->O && c.row_stride == s->row_stride;
+    if (hit) {
+        size_t off = 0;
+        for (const auto& pt : parts) {
+            if (std::memcmp(c.tables.data() + off, pt.first, pt.second * sizeof(int32_t)) != 0) {
+                hit = false;
+                break;
+            }
+            off += pt.second;
+        }
+    }
+    if (!hit) {
+        c.valid = false;
+        const int v = validate_schema(cfg, s);
+        if (v != CLEF_OK) return v;
+        c.plan = Plan();
+        build_plan(cfg, s, c.plan);
+        plan_tail_groups(c.plan, record_tail_clusters());
+        c.layout = WsLayout(cfg, c.plan);
+        c.tables.clear();
+        for (const auto& pt : parts) c.tables.insert(c.tables.end(), pt.first, pt.first + pt.second);
+        c.cfg = *cfg;
+        c.device = dev;
+        c.B = s->B;
+        c.Lpad = s->Lpad;
+        c.Q = s->Q;
+        c.O = s->O;
+        c.row_stride = s->row_stride;
+        c.valid = true;
+    }
+    *plan = &c.plan;
+    *layout = &c.layout;
+    return CLEF_OK;
+}
 
 // Clears the workspace status word and uploads the plan, both asynchronously on `st`.
 // The status word therefore reports the device-side errors of the latest call.
@@ -504,11 +570,11 @@ int clef_prepare_weights(const clef_config* cfg, const void* const* weights, voi
 int clef_workspace_size(const clef_config* cfg, const clef_schema* schema, size_t* bytes) {
     if (!bytes) return CLEF_ERR_INVALID_ARGUMENT;
     if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
-    const int v = validate_schema(cfg, schema);
+    const Plan* pp = nullptr;
+    const WsLayout* lp = nullptr;
+    const int v = cached_plan(cfg, schema, &pp, &lp);
     if (v != CLEF_OK) return v;
-    Plan p;
-    build_plan(cfg, schema, p);
-    *bytes = WsLayout(cfg, p).total;
+    *bytes = lp->total;
     return CLEF_OK;
 }
 
@@ -569,12 +635,12 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     const WIdx wi(cfg);
     for (int i = 0; i < wi.count(); ++i)
         if (!weights[i] || (reinterpret_cast<uintptr_t>(weights[i]) & 15)) return CLEF_ERR_INVALID_ARGUMENT;
-    const int v = validate_schema(cfg, schema);
+    const Plan* pp = nullptr;
+    const WsLayout* lp = nullptr;
+    const int v = cached_plan(cfg, schema, &pp, &lp);
     if (v != CLEF_OK) return v;
-    Plan p;
-    build_plan(cfg, schema, p);
-    plan_tail_groups(p, record_tail_clusters());
-    const WsLayout L(cfg, p);
+    const Plan& p = *pp;
+    const WsLayout& L = *lp;
     if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -808,14 +874,15 @@ int stream_rows_impl(const clef_config* cfg, const void* prepared, const clef_sc
     if (!prepared || !hidden || !workspace || (reinterpret_cast<uintptr_t>(hidden) & 15) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(prepared) & 255))
         return CLEF_ERR_INVALID_ARGUMENT;
-    const int v = validate_schema(cfg, schema);
+    const Plan* pp = nullptr;
+    const WsLayout* lp = nullptr;
+    const int v = cached_plan(cfg, schema, &pp, &lp);
     if (v != CLEF_OK) return v;
     if (record < 0 || record >= schema->B || row0 < 0 || n_rows < 1 ||
         int64_t(row0) + n_rows > schema->lengths[record])
         return CLEF_ERR_INVALID_ARGUMENT;
-    Plan p;
-    build_plan(cfg, schema, p);
-    const WsLayout L(cfg, p);
+    const Plan& p = *pp;
+    const WsLayout& L = *lp;
     if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -870,15 +937,13 @@ int clef_stream_begin(const clef_config* cfg, const clef_schema* schema, void* w
                       void* stream) {
     if (!config_ok(cfg)) return CLEF_ERR_UNSUPPORTED_CONFIG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return CLEF_ERR_INVALID_ARGUMENT;
-    const int v = validate_schema(cfg, schema);
+    const Plan* pp = nullptr;
+    const WsLayout* lp = nullptr;
+    const int v = cached_plan(cfg, schema, &pp, &lp);
     if (v != CLEF_OK) return v;
-    Plan p;
-    build_plan(cfg, schema, p);
-    plan_tail_groups(p, record_tail_clusters());
-    const WsLayout L(cfg, p);
-    if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < lp->total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    return upload_plan(p, ws, ws + L.plan, static_cast<cudaStream_t>(stream));
+    return upload_plan(*pp, ws, ws + lp->plan, static_cast<cudaStream_t>(stream));
 }
 
 int clef_stream_rows(const clef_config* cfg, const void* prepared, const clef_schema* schema, const uint16_t* hidden,
@@ -943,11 +1008,12 @@ int clef_span_sums(const clef_config* cfg, const clef_schema* schema, const uint
         (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(q_sum) & 15) ||
         (reinterpret_cast<uintptr_t>(o_sum) & 15) || (reinterpret_cast<uintptr_t>(x_sum) & 15))
         return CLEF_ERR_INVALID_ARGUMENT;
-    const int v = validate_schema(cfg, schema);
+    const Plan* pp = nullptr;
+    const WsLayout* lp = nullptr;
+    const int v = cached_plan(cfg, schema, &pp, &lp);
     if (v != CLEF_OK) return v;
-    Plan p;
-    build_plan(cfg, schema, p);
-    const WsLayout L(cfg, p);
+    const Plan& p = *pp;
+    const WsLayout& L = *lp;
     if (workspace_bytes < L.total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1029,10 +1095,11 @@ int clef_span_sums_noalloc(const clef_config* cfg, const clef_schema* schema, co
         (reinterpret_cast<uintptr_t>(q_sum) & 15) || (reinterpret_cast<uintptr_t>(o_sum) & 15) ||
         (reinterpret_cast<uintptr_t>(x_sum) & 15))
         return CLEF_ERR_INVALID_ARGUMENT;
-    const int v = validate_schema(cfg, schema);
+    const Plan* pp = nullptr;
+    const WsLayout* lp = nullptr;
+    const int v = cached_plan(cfg, schema, &pp, &lp);
     if (v != CLEF_OK) return v;
-    Plan p;
-    build_plan(cfg, schema, p);
+    const Plan& p = *pp;
     constexpr size_t kPlanOff = 256;  // the status word sits in the first 256 bytes
     if (kPlanOff + p.blob.size() * 4 > CLEF_SPAN_SUMS_NOALLOC_SCRATCH_BYTES) return CLEF_ERR_WORKSPACE_TOO_SMALL;
     uint8_t* scratch = nullptr;

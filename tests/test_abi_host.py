@@ -201,3 +201,27 @@ def test_selftest_wait_timeout_validation():
     assert B.clef_selftest_wait_timeout((1 << 20) + 16, 1_000_000, check=False) == 1
     assert B.clef_selftest_wait_timeout(1 << 20, 10, check=False) == 1
     assert B.clef_selftest_wait_timeout(1 << 20, 10**9, check=False) == 1
+
+
+def test_repeated_schema_is_revalidated_when_changed_in_place(small_batch):
+    """The library keeps the validated plan of the last schema it saw; a table changed in
+    place (same pointers) must be validated again, and the restored table accepted."""
+    bt = small_batch
+    cfg = B.make_config(H=256, vocab=1000)
+    sch = _schema(bt, q_span=bt.q_span.copy(), o_span=bt.o_span.copy(), lengths=bt.lengths.copy())
+    n0 = B.clef_workspace_size(cfg, sch)
+    assert B.clef_workspace_size(cfg, sch) == n0
+    os_ = sch.o_span.reshape(-1, 2)
+    keep = int(os_[0, 1])
+    os_[0, 1] = os_[0, 0]                      # empty option span, written into the same buffer
+    _expect(1, cfg, sch)
+    os_[0, 1] = keep
+    assert B.clef_workspace_size(cfg, sch) == n0
+    keep_len = int(sch.lengths[1])
+    sch.lengths[1] = bt.Lpad + 1               # longer than the padded rows
+    _expect(1, cfg, sch)
+    sch.lengths[1] = keep_len
+    assert B.clef_workspace_size(cfg, sch) == n0
+    other = _schema(bt, q_type=np.where(bt.q_type == 1, 2, bt.q_type))  # another valid schema in between
+    B.clef_workspace_size(cfg, other)
+    assert B.clef_workspace_size(cfg, sch) == n0
