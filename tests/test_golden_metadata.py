@@ -71,3 +71,26 @@ def test_response_shape_and_rounding():
     for ans in a.values():
         for v in ans.get("probabilities", {}).values():
             assert v == round(v, r["rounding_decimals"])
+
+
+HEAD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "head_config.json")))
+
+
+def _shape_fields(s):
+    return {"hidden_size": s.H, "width": s.D, "routing_layers": s.n_route, "layers": s.n_joint, "heads": s.heads,
+            "feedforward": s.F}
+
+
+def test_head_shapes_match_the_printed_configs():
+    """The generators' head shapes, the binding's default config and the wide workload
+    follow the joint_head_config.json values the pages print."""
+    import synth
+    from structured_decision_model_gb300 import binding as B
+    assert _shape_fields(synth.HeadShape()) == HEAD["flash"]
+    assert synth.HeadShape().vocab == HEAD["vocab_size"]
+    assert _shape_fields(synth.HeadShape(H=synth.workload_spec("wide_h5120_b16_l8k").H)) == HEAD["wide"]
+    c = B.make_config()
+    f = HEAD["flash"]
+    assert (c.hidden, c.width, c.n_route, c.n_joint, c.heads, c.ffn, c.vocab) == (
+        f["hidden_size"], f["width"], f["routing_layers"], f["layers"], f["heads"], f["feedforward"],
+        HEAD["vocab_size"]) and c.width // c.heads == 64
