@@ -327,17 +327,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
-                    const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+                    // descriptors of the stage's first K slice; each 16-wide slice is 32 bytes on
+                    // (2 in the descriptor's 16-byte address field)
+                    const uint64_t da = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
+                    const uint64_t db = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
                         if constexpr (PAIR)
-                            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
-                                             accum);
+                            tc_mma_bf16_pair(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, accum);
                         else
-                            tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
-                                        accum);
+                            tc_mma_bf16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, accum);
                     }
                     if constexpr (PAIR) {  // the stage is free in both CTAs once the MMAs are done
                         tc_commit_pair(smem_u32(&empty[stage]));
