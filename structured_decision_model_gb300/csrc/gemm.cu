@@ -85,12 +85,18 @@ __device__ __forceinline__ bool tile_at(const GemmArgs& a, int it, TileId& id) {
 }
 
 // PAIR: each CTA holds its 128 A rows and half (BN / 2 rows) of the pair's B tile.
+// SUB: 64-wide K slices (one 128-byte swizzle atom each) per pipeline stage.  Pairs take
+// two per stage, so that the single MMA-issuing thread waits, fences and commits once per
+// eight MMAs instead of once per four.
 template <int BN, bool PAIR>
 struct GemmCfg {
-    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int SUB = PAIR ? 2 : 1;
+    static constexpr int A_ATOM = BM * BK * 2;
+    static constexpr int A_BYTES = SUB * A_ATOM;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
-    static constexpr int B_BYTES = B_ROWS * BK * 2;
-    static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
+    static constexpr int B_ATOM = B_ROWS * BK * 2;
+    static constexpr int B_BYTES = SUB * B_ATOM;
+    static constexpr int STAGES = PAIR ? 3 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
     static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   : args.a_row_of_mtile ? args.a_row_of_mtile[id.mt] : id.mt * BM;
                 const int b_row = id.nt * BN + int(rank) * C::B_ROWS;  // pairs: this CTA's half of B
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0; kb < kb1; kb += C::SUB) {
                     const bool pre = n_pre > 0;  // stage armed and its B requested before the wait
                     if (pre) {
                         --n_pre;
@@ -279,13 +285,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // pairs: rank 0's barrier counts the stage's bytes of both CTAs
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * (C::A_BYTES + C::B_BYTES));
                     }
-                    if (PAIR && rank != 0) {
-                        const uint32_t bar = leader_full + 8u * uint32_t(stage);
-                        tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, bar);
-                        tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, bar);
-                    } else {
-                        tma_load_2d(sA + stage * C::A_BYTES, &tmA, kb * BK, a_row, &full[stage]);
-                        if (!pre) tma_load_2d(sB + stage * C::B_BYTES, &tmB, kb * BK, b_row, &full[stage]);
+#pragma unroll
+                    for (int u = 0; u < C::SUB; ++u) {
+                        if (PAIR && rank != 0) {
+                            const uint32_t bar = leader_full + 8u * uint32_t(stage);
+                            tma_load_2d_pair(sA + stage * C::A_BYTES + u * C::A_ATOM, &tmA, (kb + u) * BK, a_row, bar);
+                            tma_load_2d_pair(sB + stage * C::B_BYTES + u * C::B_ATOM, &tmB, (kb + u) * BK, b_row, bar);
+                        } else {
+                            tma_load_2d(sA + stage * C::A_BYTES + u * C::A_ATOM, &tmA, (kb + u) * BK, a_row, &full[stage]);
+                            if (!pre)
+                                tma_load_2d(sB + stage * C::B_BYTES + u * C::B_ATOM, &tmB, (kb + u) * BK, b_row,
+                                            &full[stage]);
+                        }
                     }
                     ++armed[stage];
                     if (++stage == C::STAGES) {
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0; kb < kb1; kb += C::SUB) {
                     if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.dev_flags)) {
                         ok = false;
                         break;
@@ -329,15 +340,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     // descriptors of the stage's first K slice; each 16-wide slice is 32 bytes on
                     // (2 in the descriptor's 16-byte address field)
-                    const uint64_t da = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
-                    const uint64_t db = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                        if constexpr (PAIR)
-                            tc_mma_bf16_pair(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, accum);
-                        else
-                            tc_mma_bf16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, accum);
+                    for (int u = 0; u < C::SUB; ++u) {
+                        const uint64_t da = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES + u * C::A_ATOM));
+                        const uint64_t db = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES + u * C::B_ATOM));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint32_t accum = (kb > kb0 || u > 0 || k > 0) ? 1u : 0u;
+                            if constexpr (PAIR)
+                                tc_mma_bf16_pair(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, accum);
+                            else
+                                tc_mma_bf16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, accum);
+                        }
                     }
                     if constexpr (PAIR) {  // the stage is free in both CTAs once the MMAs are done
                         tc_commit_pair(smem_u32(&empty[stage]));
