@@ -85,18 +85,19 @@ __device__ __forceinline__ bool tile_at(const GemmArgs& a, int it, TileId& id) {
 }
 
 // PAIR: each CTA holds its 128 A rows and half (BN / 2 rows) of the pair's B tile.
-// SUB: 64-wide K slices (one 128-byte swizzle atom each) per pipeline stage.  Pairs take
-// two per stage, so that the single MMA-issuing thread waits, fences and commits once per
-// eight MMAs instead of once per four.
+// SUB: 64-wide K slices (one 128-byte swizzle atom each) per pipeline stage.  Pairs and
+// the 64- and 128-wide single-CTA tiles take two per stage, so that the single
+// MMA-issuing thread waits, fences and commits once per eight MMAs instead of once per
+// four (a split's last stage holds one slice when its K-slice count is odd).
 template <int BN, bool PAIR>
 struct GemmCfg {
-    static constexpr int SUB = PAIR ? 2 : 1;
+    static constexpr int SUB = (PAIR || BN < 256) ? 2 : 1;
     static constexpr int A_ATOM = BM * BK * 2;
     static constexpr int A_BYTES = SUB * A_ATOM;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
     static constexpr int B_ATOM = B_ROWS * BK * 2;
     static constexpr int B_BYTES = SUB * B_ATOM;
-    static constexpr int STAGES = PAIR ? 3 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
+    static constexpr int STAGES = PAIR ? 3 : ((BN == 256) ? 4 : (BN == 128 ? 3 : 4));
     static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
@@ -249,10 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileId id0;
         if (args.prefetch_b && warp == 0 && lane == 0 && tile_at<PAIR>(args, 0, id0)) {
             const int kb0 = id0.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
-            n_pre = min(C::STAGES, kb1 - kb0);
+            n_pre = min(C::STAGES, (kb1 - kb0 + C::SUB - 1) / C::SUB);
             for (int i = 0; i < n_pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], C::A_BYTES + C::B_BYTES);
-                tma_load_2d(sB + i * C::B_BYTES, &tmB, (kb0 + i) * BK, id0.nt * BN, &full[i]);
+                const int kbs = kb0 + i * C::SUB, nu = min(C::SUB, kb1 - kbs);
+                mbar_arrive_expect_tx(&full[i], nu * (C::A_ATOM + C::B_ATOM));
+                for (int u = 0; u < nu; ++u)
+                    tma_load_2d(sB + i * C::B_BYTES + u * C::B_ATOM, &tmB, (kbs + u) * BK, id0.nt * BN, &full[i]);
             }
         }
     }
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b_row = id.nt * BN + int(rank) * C::B_ROWS;  // pairs: this CTA's half of B
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
                 for (int kb = kb0; kb < kb1; kb += C::SUB) {
+                    const int nu = PAIR ? C::SUB : min(C::SUB, kb1 - kb);  // K slices in this stage (pairs never split)
                     const bool pre = n_pre > 0;  // stage armed and its B requested before the wait
                     if (pre) {
                         --n_pre;
@@ -283,10 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         // pairs: rank 0's barrier counts the stage's bytes of both CTAs
-                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * (C::A_BYTES + C::B_BYTES));
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * nu * (C::A_ATOM + C::B_ATOM));
                     }
 #pragma unroll
                     for (int u = 0; u < C::SUB; ++u) {
+                        if (u >= nu) break;
                         if (PAIR && rank != 0) {
                             const uint32_t bar = leader_full + 8u * uint32_t(stage);
                             tma_load_2d_pair(sA + stage * C::A_BYTES + u * C::A_ATOM, &tmA, (kb + u) * BK, a_row, bar);
@@ -333,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
                 const int kb0 = id.sp * args.kb_per_split, kb1 = min(kb0 + args.kb_per_split, kblocks);
                 for (int kb = kb0; kb < kb1; kb += C::SUB) {
+                    const int nu = PAIR ? C::SUB : min(C::SUB, kb1 - kb);
                     if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.dev_flags)) {
                         ok = false;
                         break;
@@ -342,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // (2 in the descriptor's 16-byte address field)
 #pragma unroll
                     for (int u = 0; u < C::SUB; ++u) {
+                        if (u >= nu) break;
                         const uint64_t da = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES + u * C::A_ATOM));
                         const uint64_t db = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES + u * C::B_ATOM));
 #pragma unroll
