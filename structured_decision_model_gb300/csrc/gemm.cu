@@ -9,15 +9,22 @@
 // TMA producer, warp 1 owns TMEM and issues tcgen05.mma (one thread), warps 2..5
 // drain the fp32 accumulators from TMEM and run the epilogue.  Two TMEM
 // accumulators let the epilogue of one tile overlap the mainloop of the next.
-// Operand tiles are 64-element K slices with the 128-byte swizzle.  Tiles are
-// visited N-fastest so that CTAs working at the same time share A tiles in L2.
+// Operand tiles are 64-element K slices with the 128-byte swizzle, two per pipeline
+// stage except for single-CTA 256-wide tiles: the one MMA-issuing thread is the
+// kernel's critical path, and a stage then costs it one wait, fence and commit pair per
+// eight MMAs.  Tiles are visited N-fastest so that CTAs working at the same time share
+// A tiles in L2.
 // Operand-heavy launches of 256-wide tiles run as CTA pairs (cta_group::2): two SMs
 // compute one 256 x 256 tile, each loading half of its operands.
-// Small-M projections whose tiles cannot fill the GPU split K: the S parts of one
-// output tile run as one thread-block cluster, each stages its fp32 accumulator in
-// its own shared memory, and after a cluster barrier CTA rank r sums rows
-// [r*128/S, (r+1)*128/S) of all S staged tiles in split order through distributed
-// shared memory (deterministic, no global scratch, no CTA waits on a flag).
+// Small-M projections whose tiles cannot fill the GPU split K, in one of two ways:
+//   - cluster splits: the S parts of one output tile run as one thread-block cluster,
+//     each stages its fp32 accumulator in its own shared memory, and after a cluster
+//     barrier CTA rank r sums rows [r*128/S, (r+1)*128/S) of all S staged tiles in split
+//     order through distributed shared memory (deterministic, no global scratch, no
+//     CTA waits on a flag);
+//   - deferred splits: the S parts run as independent CTAs, each storing its raw fp32
+//     partial product into its own slab, and the kernel that consumes the projection
+//     (the LayerNorm after a residual-stream projection) sums the slabs in split order.
 // Every mbarrier wait is bounded: on a timeout the CTA sets the timeout flag,
 // waits (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
