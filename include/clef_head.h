@@ -146,7 +146,8 @@ typedef struct clef_debug_outputs {
     /* Optional cudaEvent_t handles (NULL = not recorded), recorded on `stream`
      * immediately before / after one kernel: [0] [1] the memory K/V projection GEMM,
      * [2] [3] the first routing layer's split-L attention kernel, [4] [5] span
-     * pooling, [6] [7] memory row statistics. */
+     * pooling; [6] [7] are not recorded (the memory row statistics are computed by
+     * the K/V projection, which [0] [1] bracket). */
     void* events[8];
     /* Optional launch timeline: when `timeline` is not NULL, the call records
      * timeline[k] (a cudaEvent_t) on `stream` right after its k-th kernel launch,

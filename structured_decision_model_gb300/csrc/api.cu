@@ -308,7 +308,7 @@ int partial_splits(int rows, int N, int K) {
 }
 
 struct WsLayout {
-    size_t flags, plan, mu, rstd, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf,
+    size_t flags, plan, mu, rstd, row_flags, kv, a_query, a_field, u32, x32, g32, o_res, ln_buf,
         q_buf, attn_buf, hid_buf, o_hat, f_res, f_hat, z, pm, pl, pacc, stage, part, total;
     WsLayout() = default;
     WsLayout(const clef_config* c, const Plan& p) {
@@ -329,6 +329,7 @@ struct WsLayout {
         plan = cv.take(p.blob.size() * 4);
         mu = cv.take(R * 4);
         rstd = cv.take(R * 4);
+        row_flags = cv.take(R / 4 * 8);  // publication flags of the statistics, one per 4 rows
         kv = cv.take(R * NKV * 2);
         a_query = cv.take(O * 3 * H * 2);
         a_field = cv.take(Q * (2 * H + D) * 2);
@@ -418,10 +419,13 @@ int cached_plan(const clef_config* cfg, const clef_schema* s, const Plan** plan,
     return CLEF_OK;
 }
 
-// Clears the workspace status word and uploads the plan, both asynchronously on `st`.
-// The status word therefore reports the device-side errors of the latest call.
-int upload_plan(const Plan& p, void* workspace, void* dst, cudaStream_t st) {
+// Clears the workspace status word (and, when given, the statistics' publication
+// flags) and uploads the plan, all asynchronously on `st`.  The status word therefore
+// reports the device-side errors of the latest call.
+int upload_plan(const Plan& p, void* workspace, void* dst, cudaStream_t st, void* row_flags = nullptr,
+                size_t row_flags_bytes = 0) {
     if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return CLEF_ERR_CUDA;
+    if (row_flags && cudaMemsetAsync(row_flags, 0, row_flags_bytes, st) != cudaSuccess) return CLEF_ERR_CUDA;
     if (launch_plan_upload(static_cast<int32_t*>(dst), p.blob.data(), p.blob.size(), st) != cudaSuccess)
         return CLEF_ERR_CUDA;
     return CLEF_OK;
@@ -660,7 +664,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     const int B = p.B, Q = p.Q, O = p.O;
 
     if (mode == kForwardFull) {
-        const int u = upload_plan(p, ws, ws + L.plan, st);
+        const int u = upload_plan(p, ws, ws + L.plan, st, ws + L.row_flags, size_t(p.R) / 4 * 8);
         if (u != CLEF_OK) return u;
     }
     auto T = [&](size_t off) { return plan + off; };
@@ -695,12 +699,28 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     };
     int splits = 1;
 
-    // 1. memory row statistics (the memory LayerNorm is applied through them)
-    if (mode == kForwardFull) {
-        CK(mark(debug, 6, st));
-        CK(launch_row_stats(hidden, schema->row_stride, schema->Lpad, H, T(p.tile_rec), T(p.rec_row_off),
-                            T(p.lengths), p.R, mu, rstd, st)); CK(tick());
-        CK(mark(debug, 7, st));
+    // 1. memory K/V of every routing layer (LayerNorm folded), real rows only; the
+    // projection also writes the memory row statistics that pooling applies the memory
+    // LayerNorm through
+    if (mode == kForwardAfterStream) {
+        // K/V rows and statistics came in chunk by chunk; the round-up slack rows of each
+        // record were never written, and attention reads whole tiles, so they are zeroed here
+        CK(launch_zero_slack(kv, NKV, T(p.rec_row_off), T(p.lengths), B, st)); CK(tick());
+    } else {
+        GemmProblem g;
+        g.A = hidden; g.lda = schema->row_stride; g.a_rows = int64_t(B) * schema->Lpad;
+        g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
+        g.N = NKV; g.K = H; g.n_mtiles = p.n_mtiles; g.a_row_of_mtile = T(p.tile_a_row);
+        GemmEpilogue e;
+        e.kind = EPI_KV_LNFOLD; e.row_mu = mu; e.row_rstd = rstd;
+        e.tile_rec = T(p.tile_rec); e.rec_row_off = T(p.rec_row_off); e.rec_len = T(p.lengths);
+        e.row_flags = reinterpret_cast<uint64_t*>(ws + L.row_flags);
+        e.col_c = reinterpret_cast<const float*>(pw + PL.ckv);
+        e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
+        e.out = kv; e.ldo = NKV; e.M = p.R;
+        CK(mark(debug, 0, st));
+        CK(launch_gemm(g, e, flags, st)); CK(tick());
+        CK(mark(debug, 1, st));
     }
     // 2. span pooling
     SpanPoolArgs sp{};
@@ -725,25 +745,6 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
                      &splits)); CK(tick());
     const uint16_t* pending_bias = W(weights, 5);  // bias of the projection whose partials are in `part`
     bool pending_resid = false;
-    // 4. memory K/V of every routing layer (LayerNorm folded), real rows only
-    if (mode == kForwardAfterStream) {
-        // K/V rows came in chunk by chunk; the round-up slack rows of each record were never
-        // written, and attention reads whole tiles, so they are zeroed here
-        CK(launch_zero_slack(kv, NKV, T(p.rec_row_off), T(p.lengths), B, st)); CK(tick());
-    } else {
-        GemmProblem g;
-        g.A = hidden; g.lda = schema->row_stride; g.a_rows = int64_t(B) * schema->Lpad;
-        g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
-        g.N = NKV; g.K = H; g.n_mtiles = p.n_mtiles; g.a_row_of_mtile = T(p.tile_a_row);
-        GemmEpilogue e;
-        e.kind = EPI_KV_LNFOLD; e.row_mu = mu; e.row_rstd = rstd;
-        e.col_c = reinterpret_cast<const float*>(pw + PL.ckv);
-        e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
-        e.out = kv; e.ldo = NKV; e.M = p.R;
-        CK(mark(debug, 0, st));
-        CK(launch_gemm(g, e, flags, st)); CK(tick());
-        CK(mark(debug, 1, st));
-    }
     // 5. evidence routing layers
     RouteAttnArgs ra{};
     ra.q = q_buf; ra.ldq = D; ra.kv = kv; ra.ldkv = NKV; ra.kv_rows = p.R; ra.heads = cfg->heads; ra.flags = flags;
@@ -865,8 +866,9 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
 }
 
 // Statistics and K/V of rows [row0, row0 + n_rows) of one record.  fp16 rows are first
-// rounded to bf16 into the workspace staging area, kStageRows at a time; the statistics
-// and the projection then read that copy, exactly as they read bf16 rows.
+// rounded to bf16 into the workspace staging area, kStageRows at a time; the projection
+// (which computes the statistics from the rows it stages) then reads that copy, exactly
+// as it reads bf16 rows.
 int stream_rows_impl(const clef_config* cfg, const void* prepared, const clef_schema* schema, const uint16_t* hidden,
                      int32_t record, int32_t row0, int32_t n_rows, void* workspace, size_t workspace_bytes,
                      void* stream, bool f16) {
@@ -904,13 +906,13 @@ int stream_rows_impl(const clef_config* cfg, const void* prepared, const clef_sc
         const int64_t out_row = out_row0 + done;
         float* mu = reinterpret_cast<float*>(ws + L.mu) + out_row;
         float* rstd = reinterpret_cast<float*>(ws + L.rstd) + out_row;
-        CK(launch_row_stats_rows(rows, ld, H, n, mu, rstd, st));
         GemmProblem g;
         g.A = rows; g.lda = ld; g.a_rows = n;
         g.B = reinterpret_cast<const uint16_t*>(pw + PL.wkv); g.ldb = H;
         g.N = NKV; g.K = H; g.n_mtiles = (n + kTile - 1) / kTile;
         GemmEpilogue e;
         e.kind = EPI_KV_LNFOLD; e.row_mu = mu; e.row_rstd = rstd;
+        e.row_flags = reinterpret_cast<uint64_t*>(ws + L.row_flags);  // rows of this call's tiles
         e.col_c = reinterpret_cast<const float*>(pw + PL.ckv);
         e.bias_f32 = reinterpret_cast<const float*>(pw + PL.bkv);
         e.out = reinterpret_cast<uint16_t*>(ws + L.kv) + out_row * NKV; e.ldo = NKV; e.M = n;
@@ -943,7 +945,8 @@ int clef_stream_begin(const clef_config* cfg, const clef_schema* schema, void* w
     if (v != CLEF_OK) return v;
     if (workspace_bytes < lp->total) return CLEF_ERR_WORKSPACE_TOO_SMALL;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    return upload_plan(*pp, ws, ws + lp->plan, static_cast<cudaStream_t>(stream));
+    return upload_plan(*pp, ws, ws + lp->plan, static_cast<cudaStream_t>(stream), ws + lp->row_flags,
+                       size_t(pp->R) / 4 * 8);
 }
 
 int clef_stream_rows(const clef_config* cfg, const void* prepared, const clef_schema* schema, const uint16_t* hidden,

@@ -167,6 +167,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Publishes `value` in a global flag (release at GPU scope: what this thread wrote, and
+// what it has seen written, before the call is visible to a thread that reads the value
+// through flag_wait_bounded).
+__device__ __forceinline__ void flag_publish(uint64_t* flag, uint64_t value) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(value) : "memory");
+}
+
+// Bounded wait (acquire at GPU scope) until a global flag holds `value`: written by
+// another CTA of the same launch, which the launch keeps resident alongside the waiting
+// one.  Returns false on a timeout (setting the timeout flag) or at once once another
+// role of the CTA has aborted.
+__device__ __forceinline__ bool flag_wait_bounded(const uint64_t* flag, uint64_t value, volatile int* abort_flag,
+                                                  int* dev_flags, uint64_t limit_ns = kWaitLimitNs) {
+    uint64_t start = 0;
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        uint64_t v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(flag) : "memory");
+        if (v == value) return true;
+        if (abort_flag && *abort_flag) return false;
+        const uint64_t now = global_ns();
+        if (start == 0) start = now;
+        else if (now - start > limit_ns) break;
+        __nanosleep(128);
+    }
+    if (abort_flag) *abort_flag = 1;
+    if (dev_flags) atomicOr(dev_flags, kFlagTimeout);
+    return false;
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,

@@ -25,6 +25,12 @@
 //   - deferred splits: the S parts run as independent CTAs, each storing its raw fp32
 //     partial product into its own slab, and the kernel that consumes the projection
 //     (the LayerNorm after a residual-stream projection) sums the slabs in split order.
+// The K/V projection's kernels carry four more warps that compute the memory LayerNorm
+// statistics of A's rows while the tensor cores run: jobs of 16 rows, spread over every
+// CTA of the launch and paced by its producer, read from L2 just ahead of the GEMM's own
+// copies of the rows (shared memory has no bandwidth to spare next to the MMAs), each
+// warp publishing its 4 rows through a flag that the epilogues of every tile of those
+// rows wait for before applying the fold.  The rows are read from HBM once.
 // Every mbarrier wait is bounded: on a timeout the CTA sets the timeout flag,
 // waits (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
@@ -40,7 +46,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+constexpr int kStatsWarps = 4;  // LayerNorm-statistics warps of the K/V projection's kernels
 constexpr int kMaxSplits = 4;  // cluster size of a split-K tile (8-CTA clusters did not all fit at once)
 
 struct GemmArgs {
@@ -54,6 +60,8 @@ struct GemmArgs {
     int prefetch_b;                // B tiles of the first stages may be requested before the PDL wait
     int deferred;                  // split-K without a cluster: split sp stores its raw partial
     int64_t part_stride;           // into slab sp (elements between slabs) of the epilogue output
+    const uint16_t* a_ptr;         // LN fold: A itself (row stride lda elements), read by the
+    int64_t lda;                   // statistics jobs
 };
 
 // Tile t of the persistent walk: split fastest, then N, then M.
@@ -96,8 +104,11 @@ __device__ __forceinline__ bool tile_at(const GemmArgs& a, int it, TileId& id) {
 // the 64- and 128-wide single-CTA tiles take two per stage, so that the single
 // MMA-issuing thread waits, fences and commits once per eight MMAs instead of once per
 // four (a split's last stage holds one slice when its K-slice count is odd).
-template <int BN, bool PAIR>
+// STATS: the kernel also computes the LayerNorm statistics of its A rows (the K/V
+// projection with the memory LayerNorm folded in).
+template <int BN, bool PAIR, bool STATS>
 struct GemmCfg {
+    static constexpr int THREADS = 192 + (STATS ? 32 * kStatsWarps : 0);
     static constexpr int SUB = (PAIR || BN < 256) ? 2 : 1;
     static constexpr int A_ATOM = BM * BK * 2;
     static constexpr int A_BYTES = SUB * A_ATOM;
@@ -109,14 +120,14 @@ struct GemmCfg {
     static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
 
+// Columns n0 .. n0 + 15 of row m; mu and rs are the row's LayerNorm statistics (LN fold).
 template <int BN>
 __device__ __forceinline__ void epilogue_chunk(const GemmEpilogue& e, int m, int n0, const uint32_t (&r)[16],
-                                               int64_t slab = 0) {
+                                               int64_t slab, float mu, float rs) {
     float v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
     if (e.kind == EPI_KV_LNFOLD) {
-        const float mu = e.row_mu[m], rs = e.row_rstd[m];
         // rstd == 0 marks a row of a record's round-up slack: stored as zeros, so that
         // whatever the padding held never reaches attention as a non-finite value
 #pragma unroll
@@ -188,6 +199,43 @@ __device__ __forceinline__ void epilogue_chunk_split(const GemmEpilogue& e, int 
     }
 }
 
+// Memory LayerNorm statistics (mean, 1/sqrt(var + eps)) of one bf16 row of K values, by
+// the 8 threads of an aligned 8-lane group (`part` = lane & 7).  The row's values are
+// taken less a shift (the mean of its first 8 values, which keeps the fp32 sums free
+// of cancellation for rows far from zero mean); thread `part` sums and square-sums the
+// 16-byte chunks part, part + 8, ... over two interleaved accumulators, and the group
+// adds its 8 partial sums in a butterfly (every lane ends with the same bits).  The
+// loads go through L2 (not L1): the GEMM's own copies of the same rows follow shortly
+// and find them there.
+__device__ __forceinline__ float2 row_moments(const uint16_t* row, int K, int part, unsigned group_mask) {
+    const uint4* rp = reinterpret_cast<const uint4*>(row);
+    const uint4 h = __ldcg(rp);
+    const float shift = ((bf16_lo(h.x) + bf16_hi(h.x)) + (bf16_lo(h.y) + bf16_hi(h.y)) +
+                         ((bf16_lo(h.z) + bf16_hi(h.z)) + (bf16_lo(h.w) + bf16_hi(h.w)))) * 0.125f;
+    float s0 = 0.f, s1 = 0.f, q0 = 0.f, q1 = 0.f;
+    const int n16 = K >> 3;
+#pragma unroll 8
+    for (int c = part; c < n16; c += 8) {
+        const uint4 v = __ldcg(rp + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float d0 = bf16_lo(w[i]) - shift, d1 = bf16_hi(w[i]) - shift;
+            s0 += d0; q0 = fmaf(d0, d0, q0);
+            s1 += d1; q1 = fmaf(d1, d1, q1);
+        }
+    }
+    float s = s0 + s1, q = q0 + q1;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        s += __shfl_xor_sync(group_mask, s, o);
+        q += __shfl_xor_sync(group_mask, q, o);
+    }
+    s /= float(K);
+    q /= float(K);
+    return make_float2(shift + s, rsqrtf(fmaxf(q - s * s, 0.f) + 1e-5f));
+}
+
 // PAIR (CTA pairs on cta_group::2) is only launched without split-K.
 //
 // CTA pairs.  Each CTA's producer loads its own A tile (128 rows) and its half of the
@@ -199,11 +247,11 @@ __device__ __forceinline__ void epilogue_chunk_split(const GemmEpilogue& e, int 
 // both; the epilogue warps of both CTAs arrive on rank 0's `tempty`.  Rank 1 cannot
 // observe its own copies land (they complete on rank 0), so it leaves only through
 // the final cluster barrier, after rank 0 has consumed or waited for every stage.
-template <int BN, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, bool PAIR, bool STATS>
+__global__ void __launch_bounds__(GemmCfg<BN, PAIR, STATS>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args) {
-    using C = GemmCfg<BN, PAIR>;
+    using C = GemmCfg<BN, PAIR, STATS>;
     constexpr int kRedLd = BN + 4;  // staged split-K row stride (floats): conflict-free float4 rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -216,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* load_mt = abort_flag + 1;  // STATS: M tile the producer is loading (INT_MAX: done)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // rank 1 of a pair issues no MMA
@@ -230,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *load_mt = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -279,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             TileId id;
             for (int it = 0; ok && tile_at<PAIR>(args, it, id); ++it) {
+                if (STATS) *load_mt = id.mt;
                 const int a_row = id.mt >= args.n_mtiles ? args.a_rows
                                   : args.a_row_of_mtile ? args.a_row_of_mtile[id.mt] : id.mt * BM;
                 const int b_row = id.nt * BN + int(rank) * C::B_ROWS;  // pairs: this CTA's half of B
@@ -318,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (STATS) *load_mt = 0x7fffffff;
             if (!ok && rank == 0) {  // let every copy this CTA's barriers count land before it exits
                 for (int s = 0; s < C::STAGES; ++s)
                     if (armed[s] != 0) mbar_wait_bounded(&full[s], (armed[s] - 1) & 1u, nullptr, nullptr);
@@ -394,6 +446,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(drain, 0, nullptr, args.dev_flags);
         }
         __syncwarp();
+    } else if (STATS && warp >= 6) {
+        // LayerNorm statistics jobs: job j covers rows (j % 8) * 16 .. + 15 of 128-row tile
+        // j / 8; the jobs are dealt round-robin over the launch's CTAs in tile order.  8
+        // threads per row; warp w of the four publishes rows 4w .. 4w + 3 of the job.
+        // Pacing: a job for tile mt starts once this CTA's producer is loading an M tile
+        // of at least mt.  With the jobs dealt in tile order, each CTA's jobs then run
+        // about when the GEMM reaches their rows: the rows stream in alongside the GEMM's
+        // own operand copies (which find them in L2) instead of in one burst ahead of
+        // them, and a job still ends well inside the mainloop of its tiles.  The rule
+        // cannot deadlock: the producer's way to its first tile of M index mt or more only
+        // waits on epilogues of tiles below mt, whose jobs come earlier.
+        const int t = int(threadIdx.x) - 192;
+        const int part = t & 7;
+        const unsigned group_mask = 0xffu << (lane & 24);
+        const int n_jobs = args.n_mtiles * 8;
+        bool ok = true;
+        for (int j = int(blockIdx.x); ok && j < n_jobs; j += int(gridDim.x)) {
+            const int mt = j >> 3, r = (j & 7) * 16 + (t >> 3), m = mt * BM + r;
+            const uint64_t t0 = global_ns();
+            while (*load_mt < mt) {  // each lane on its own, then all lanes agree
+                if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(256);
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            bool real = m < args.epi.M;
+            if (real && args.epi.tile_rec) {
+                const int b = args.epi.tile_rec[mt];
+                real = m - args.epi.rec_row_off[b] < args.epi.rec_len[b];
+            }
+            float2 st = make_float2(0.f, 0.f);  // padding rows: mu = rstd = 0
+            if (real) {
+                const int64_t a_row = (args.a_row_of_mtile ? args.a_row_of_mtile[mt] : mt * BM) + r;
+                st = row_moments(args.a_ptr + a_row * args.lda, args.kblocks * BK, part, group_mask);
+            }
+            if (part == 0 && m < args.epi.M) {
+                args.epi.row_mu[m] = st.x;
+                args.epi.row_rstd[m] = st.y;
+                __threadfence();  // the rows' statistics reach GPU scope before the flag
+            }
+            __syncwarp();
+            if (lane == 0) flag_publish(args.epi.row_flags + (j * 4 + (warp - 6)), args.epi.epoch);
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(args.dev_flags, kFlagTimeout);
+        }
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may read
         const int r_in_tile = quarter * 32 + lane;
@@ -422,6 +526,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int m = id.mt * BM + r_in_tile;
             const bool store = m < args.epi.M;
+            float row_mu = 0.f, row_rs = 0.f;
+            if constexpr (STATS) {  // this row's LayerNorm statistics, once its job has published them
+                const bool got = !store || flag_wait_bounded(args.epi.row_flags + (m >> 2), args.epi.epoch,
+                                                             abort_flag, args.dev_flags);
+                if (!__all_sync(0xffffffffu, got)) break;
+                if (store) {
+                    row_mu = __ldcg(args.epi.row_mu + m);
+                    row_rs = __ldcg(args.epi.row_rstd + m);
+                }
+            }
             if (args.splits == 1 || args.deferred) {
                 const int64_t slab = args.deferred ? int64_t(id.sp) * args.part_stride : 0;
 #pragma unroll 1
@@ -429,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[16];
                     tmem_ld16(tmem_base + uint32_t(acc * BN + c * 16) + (uint32_t(quarter * 32) << 16), r);
                     tmem_ld_wait();
-                    if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r, slab);
+                    if (store) epilogue_chunk<BN>(args.epi, m, id.nt * BN + c * 16, r, slab, row_mu, row_rs);
                 }
                 tc_fence_before();
                 if constexpr (PAIR) {
@@ -464,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    if (!PAIR && args.splits > 1 && !args.deferred) {
+    if (!PAIR && !STATS && args.splits > 1 && !args.deferred) {
         // every thread of every CTA of the cluster passes both barriers, on every path
         cluster_sync();
         if (warp >= 2) {
@@ -557,21 +671,21 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 namespace {
 
 // Opts the kernel into its dynamic shared memory size (once per instantiation).
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool STATS>
 cudaError_t kernel_attributes() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   GemmCfg<BN, PAIR>::SMEM);
+        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, PAIR, STATS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   GemmCfg<BN, PAIR, STATS>::SMEM);
     });
     return err;
 }
 
 // How many clusters of `size` CTAs of this kernel the GPU holds at once (0: none).
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool STATS>
 int active_clusters(int size) {
-    if (kernel_attributes<BN, PAIR>() != cudaSuccess) return 0;
+    if (kernel_attributes<BN, PAIR, STATS>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -579,12 +693,12 @@ int active_clusters(int size) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(size);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = GemmCfg<BN, PAIR>::SMEM;
+    cfg.blockDim = dim3(GemmCfg<BN, PAIR, STATS>::THREADS);
+    cfg.dynamicSmemBytes = GemmCfg<BN, PAIR, STATS>::SMEM;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, PAIR>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, PAIR, STATS>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -599,7 +713,7 @@ int max_cluster_splits() {
     static int best = 1;
     std::call_once(once, [] {
         for (int S = kMaxSplits; S > 1; S >>= 1) {
-            if (active_clusters<BN, false>(S) > 0) {
+            if (active_clusters<BN, false, false>(S) > 0) {
                 best = S;
                 break;
             }
@@ -609,15 +723,17 @@ int max_cluster_splits() {
 }
 
 // CTA pairs of the BN = 256 pair kernel the GPU holds at once (0: the mode is unavailable).
+template <bool STATS>
 int pair_clusters() {
     static std::once_flag once;
     static int n = 0;
-    std::call_once(once, [] { n = active_clusters<256, true>(2); });
+    std::call_once(once, [] { n = active_clusters<256, true, STATS>(2); });
     return n;
 }
 
-cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, GemmArgs), int grid, int cluster, size_t smem,
-                           cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a) {
+cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, GemmArgs), int grid, int cluster, int threads,
+                           size_t smem, cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const GemmArgs& a) {
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -627,7 +743,7 @@ cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, GemmArgs), i
     attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -640,9 +756,10 @@ cudaError_t launch_cluster(void (*kernel)(CUtensorMap, CUtensorMap, GemmArgs), i
 // 128 A rows and 128 of the 256 B rows, which cuts the L2-to-SM operand traffic per K
 // block from 48 KB to 32 KB per CTA.  Returns false (nothing launched) when the GPU
 // cannot hold a pair of this kernel.
+template <bool STATS>
 bool launch_pair(const GemmProblem& p, const GemmArgs& a, cudaStream_t s, const CUtensorMap& ta, cudaError_t* err) {
-    using C = GemmCfg<256, true>;
-    const int clusters = pair_clusters();
+    using C = GemmCfg<256, true, STATS>;
+    const int clusters = pair_clusters<STATS>();
     if (clusters <= 0) return false;
     CUtensorMap tbh;  // B in 128-row boxes: this CTA's half of the pair's B tile
     if (!make_tma_2d_bf16(&tbh, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), C::B_ROWS)) {
@@ -651,15 +768,15 @@ bool launch_pair(const GemmProblem& p, const GemmArgs& a, cudaStream_t s, const 
     }
     const int groups = (a.n_mtiles + 1) / 2 * a.n_ntiles;
     const int grid = 2 * std::min(groups, clusters);
-    *err = launch_cluster(gemm_tc_kernel<256, true>, grid, 2, C::SMEM, s, ta, tbh, a);
+    *err = launch_cluster(gemm_tc_kernel<256, true, STATS>, grid, 2, C::THREADS, C::SMEM, s, ta, tbh, a);
     return true;
 }
 
-template <int BN>
+template <int BN, bool STATS>
 cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, cudaStream_t s, int splits,
                       bool deferred = false) {
-    using C = GemmCfg<BN, false>;
-    const cudaError_t attr_err = kernel_attributes<BN, false>();
+    using C = GemmCfg<BN, false, STATS>;
+    const cudaError_t attr_err = kernel_attributes<BN, false, STATS>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ta, tb;
     if (!make_tma_2d_bf16(&ta, p.A, uint64_t(p.K), uint64_t(p.a_rows), uint64_t(p.lda), BM)) return cudaErrorInvalidValue;
@@ -676,6 +793,8 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
     a.prefetch_b = p.b_is_weight ? 1 : 0;
     a.deferred = deferred ? 1 : 0;
     a.part_stride = p.part_stride;
+    a.a_ptr = p.A;
+    a.lda = p.lda;
     const int sms = num_sms();
     const int out_tiles = a.n_mtiles * a.n_ntiles;
     const int tiles = out_tiles * a.splits;
@@ -683,15 +802,15 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmEpilogue& e, int* flags, c
         if (a.splits == 1 && !deferred && out_tiles > sms) {
             a.prefetch_b = 0;
             cudaError_t err = cudaSuccess;
-            if (launch_pair(p, a, s, ta, &err)) return err;
+            if (launch_pair<STATS>(p, a, s, ta, &err)) return err;
             a.prefetch_b = p.b_is_weight ? 1 : 0;
         }
     }
     if (!make_tma_2d_bf16(&tb, p.B, uint64_t(p.K), uint64_t(p.N), uint64_t(p.ldb), BN)) return cudaErrorInvalidValue;
     if (a.splits > 1 && !deferred)  // one CTA per (output tile, split); the splits of a tile form one cluster
-        return launch_cluster(gemm_tc_kernel<BN, false>, tiles, a.splits, C::SMEM, s, ta, tb, a);
+        return launch_cluster(gemm_tc_kernel<BN, false, STATS>, tiles, a.splits, C::THREADS, C::SMEM, s, ta, tb, a);
     const int grid = tiles < sms ? tiles : sms;
-    return launch_pdl(gemm_tc_kernel<BN, false>, dim3(grid), dim3(kThreads), C::SMEM, s, ta, tb, a);
+    return launch_pdl(gemm_tc_kernel<BN, false, STATS>, dim3(grid), dim3(C::THREADS), C::SMEM, s, ta, tb, a);
 }
 
 }  // namespace
@@ -744,10 +863,31 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_fl
             p.N % p.defer_bn)
             return cudaErrorInvalidValue;
         switch (p.defer_bn) {
-            case 256: return launch_bn<256>(p, e, dev_flags, s, p.defer_splits, true);
-            case 128: return launch_bn<128>(p, e, dev_flags, s, p.defer_splits, true);
-            case 64: return launch_bn<64>(p, e, dev_flags, s, p.defer_splits, true);
+            case 256: return launch_bn<256, false>(p, e, dev_flags, s, p.defer_splits, true);
+            case 128: return launch_bn<128, false>(p, e, dev_flags, s, p.defer_splits, true);
+            case 64: return launch_bn<64, false>(p, e, dev_flags, s, p.defer_splits, true);
             default: return cudaErrorInvalidValue;
+        }
+    }
+    if (e.kind == EPI_KV_LNFOLD) {
+        // the LN fold computes its row statistics in the kernel: never split, every row's
+        // output tiles see its whole K range
+        if (p.allow_split || !e.row_mu || !e.row_rstd || !e.row_flags) return cudaErrorInvalidValue;
+        const int sms = num_sms();
+        int bn = force_bn;
+        if (bn == 0) {
+            bn = 64;
+            if (p.N % 256 == 0 && p.n_mtiles * (p.N / 256) >= sms) bn = 256;
+            else if (p.N % 128 == 0 && p.n_mtiles * (p.N / 128) >= sms) bn = 128;
+        }
+        if (p.N % bn != 0) return cudaErrorInvalidValue;
+        static std::atomic<uint64_t> epochs{0};
+        GemmEpilogue ef = e;
+        ef.epoch = epochs.fetch_add(1, std::memory_order_relaxed) + 1;  // never 0, the cleared value
+        switch (bn) {
+            case 256: return launch_bn<256, true>(p, ef, dev_flags, s, 1);
+            case 128: return launch_bn<128, true>(p, ef, dev_flags, s, 1);
+            default: return launch_bn<64, true>(p, ef, dev_flags, s, 1);
         }
     }
     const int sms = num_sms();
@@ -785,9 +925,9 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmEpilogue& e, int* dev_fl
     }
     if (p.N % bn != 0) return cudaErrorInvalidValue;
     switch (bn) {
-        case 256: return launch_bn<256>(p, e, dev_flags, s, splits);
-        case 128: return launch_bn<128>(p, e, dev_flags, s, splits);
-        default: return launch_bn<64>(p, e, dev_flags, s, splits);
+        case 256: return launch_bn<256, false>(p, e, dev_flags, s, splits);
+        case 128: return launch_bn<128, false>(p, e, dev_flags, s, splits);
+        default: return launch_bn<64, false>(p, e, dev_flags, s, splits);
     }
 }
 

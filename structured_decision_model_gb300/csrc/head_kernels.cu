@@ -1,4 +1,4 @@
-// The head's non-GEMM kernels: memory row statistics, span pooling, LayerNorm of
+// The head's non-GEMM kernels: span pooling, LayerNorm of
 // the option / field streams, split-L routing attention and its merge, field
 // aggregation, field self-attention, scorer input assembly, scoring with the
 // per-question softmax, and the weight-preparation kernels.
@@ -7,82 +7,6 @@
 #include "kernels.h"
 
 namespace clef {
-
-// =====================================================================
-// Memory row statistics: mean and 1/sqrt(var + eps) of every real hidden row,
-// indexed by compact row (record rows padded up to a 128-row boundary).  The
-// memory LayerNorm ("clef-flash-CoreAI metadata.json" decision.head.reads) is
-// applied through these statistics by the K/V projection epilogue and by pooling.
-// Rows in a record's round-up slack get mu = rstd = 0.
-// =====================================================================
-// Mean and 1/sqrt(var + eps) of one bf16 row (one warp; two passes over the row, the
-// second served from L1).
-__device__ __forceinline__ void row_moments(const uint16_t* __restrict__ rowp, int H, int lane, float& mean,
-                                            float& rstd_out) {
-    const uint4* row = reinterpret_cast<const uint4*>(rowp);
-    const int n8 = H >> 3;
-    float s = 0.f;
-#pragma unroll 4
-    for (int i = lane; i < n8; i += 32) {
-        uint4 w = __ldg(row + i);
-        s += bf16_lo(w.x) + bf16_hi(w.x) + bf16_lo(w.y) + bf16_hi(w.y) + bf16_lo(w.z) + bf16_hi(w.z) +
-             bf16_lo(w.w) + bf16_hi(w.w);
-    }
-    const float m = warp_sum(s) / float(H);
-    float q = 0.f;
-#pragma unroll 4
-    for (int i = lane; i < n8; i += 32) {
-        uint4 w = __ldg(row + i);
-        float d;
-        d = bf16_lo(w.x) - m; q += d * d; d = bf16_hi(w.x) - m; q += d * d;
-        d = bf16_lo(w.y) - m; q += d * d; d = bf16_hi(w.y) - m; q += d * d;
-        d = bf16_lo(w.z) - m; q += d * d; d = bf16_hi(w.z) - m; q += d * d;
-        d = bf16_lo(w.w) - m; q += d * d; d = bf16_hi(w.w) - m; q += d * d;
-    }
-    mean = m;
-    rstd_out = rsqrtf(warp_sum(q) / float(H) + 1e-5f);
-}
-
-__global__ void __launch_bounds__(256) row_stats_kernel(const uint16_t* __restrict__ hidden, int64_t row_stride,
-                                                       int Lpad, int H, const int32_t* __restrict__ tile_rec,
-                                                       const int32_t* __restrict__ rec_row_off,
-                                                       const int32_t* __restrict__ lengths, int R,
-                                                       float* __restrict__ mu, float* __restrict__ rstd) {
-    griddep_wait();
-    griddep_launch();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 8 + warp;
-    if (r >= R) return;
-    const int b = tile_rec[r >> 7];
-    const int t = r - rec_row_off[b];
-    if (t >= lengths[b]) {
-        if (lane == 0) { mu[r] = 0.f; rstd[r] = 0.f; }
-        return;
-    }
-    float m, rs;
-    row_moments(hidden + (int64_t(b) * Lpad + t) * row_stride, H, lane, m, rs);
-    if (lane == 0) {
-        mu[r] = m;
-        rstd[r] = rs;
-    }
-}
-
-// Statistics of n consecutive real rows (streamed memory rows of one record).
-__global__ void __launch_bounds__(256) row_stats_rows_kernel(const uint16_t* __restrict__ rows, int64_t row_stride,
-                                                            int H, int n, float* __restrict__ mu,
-                                                            float* __restrict__ rstd) {
-    griddep_wait();
-    griddep_launch();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 8 + warp;
-    if (r >= n) return;
-    float m, rs;
-    row_moments(rows + int64_t(r) * row_stride, H, lane, m, rs);
-    if (lane == 0) {
-        mu[r] = m;
-        rstd[r] = rs;
-    }
-}
 
 // fp16 rows [rows][H] (row stride ld_src) rounded to a dense bf16 copy [rows][H]: the
 // streaming path's fp16 input, 8 values (16 bytes) per thread.
@@ -757,20 +681,6 @@ __global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(int* flags, u
 cudaError_t launch_wait_timeout_selftest(int* flags, uint64_t limit_ns, cudaStream_t s) {
     wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(flags, limit_ns);
     return counted(cudaGetLastError());
-}
-
-cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpad, int H, const int32_t* tile_rec,
-                             const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,
-                             cudaStream_t s) {
-    if (R <= 0) return cudaSuccess;
-    return launch_pdl(row_stats_kernel, dim3((R + 7) / 8), dim3(256), 0, s, hidden, row_stride, Lpad, H, tile_rec,
-                      rec_row_off, lengths, R, mu, rstd);
-}
-
-cudaError_t launch_row_stats_rows(const uint16_t* rows, int64_t row_stride, int H, int n, float* mu, float* rstd,
-                                  cudaStream_t s) {
-    if (n <= 0) return cudaSuccess;
-    return launch_pdl(row_stats_rows_kernel, dim3((n + 7) / 8), dim3(256), 0, s, rows, row_stride, H, n, mu, rstd);
 }
 
 cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off, const int32_t* lengths, int B,

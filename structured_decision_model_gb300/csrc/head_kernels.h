@@ -121,11 +121,6 @@ cudaError_t launch_record_tail(const RecordTailArgs& a, cudaStream_t s);
 // q / k / v matrix (qkv = 1, R = 3 * 64), row (j / 64) D + 64 r + j % 64.
 cudaError_t launch_tail_slices(const uint16_t* w, int K, int R, int qkv, int D, uint16_t* dst, cudaStream_t s);
 
-cudaError_t launch_row_stats(const uint16_t* hidden, int64_t row_stride, int Lpad, int H, const int32_t* tile_rec,
-                             const int32_t* rec_row_off, const int32_t* lengths, int R, float* mu, float* rstd,
-                             cudaStream_t s);
-cudaError_t launch_row_stats_rows(const uint16_t* rows, int64_t row_stride, int H, int n, float* mu, float* rstd,
-                                  cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(int* flags, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_zero_slack(uint16_t* kv, int ldkv, const int32_t* rec_row_off, const int32_t* lengths, int B,
                               cudaStream_t s);

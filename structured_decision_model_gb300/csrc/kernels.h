@@ -41,7 +41,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 enum EpiKind : int {
     EPI_F32 = 0,        // out_f32 = acc + bias
     EPI_BF16 = 2,       // out_bf16 = act(acc + bias)
-    EPI_KV_LNFOLD = 3,  // out_bf16 = rstd[m] * (acc - mu[m] * col_c[n]) + bias_f32[n]
+    EPI_KV_LNFOLD = 3,  // out_bf16 = rstd[m] * (acc - mu[m] * col_c[n]) + bias_f32[n], with mu and
+                        // rstd the memory LayerNorm statistics of A's row m, computed in the kernel
 };
 
 struct GemmEpilogue {
@@ -49,8 +50,20 @@ struct GemmEpilogue {
     int gelu = 0;
     const uint16_t* bias_bf16 = nullptr;  // [N]
     const float* bias_f32 = nullptr;      // [N]
-    const float* row_mu = nullptr;        // [rows] (LN fold)
-    const float* row_rstd = nullptr;      // [rows] (LN fold)
+    // LN fold: the row statistics are written to row_mu / row_rstd for rows m < M.  With
+    // tile_rec given, row m belongs to record b = tile_rec[m / 128] and is a padding row
+    // when m - rec_row_off[b] >= rec_len[b] (without: every row m < M is real); padding
+    // rows get mu = rstd = 0 and are stored as zeros.  row_flags[m / 4] (n_mtiles * 32 entries)
+    // is set to `epoch` once rows m .. m + 3 are published; the launcher assigns each
+    // launch a new epoch, so the flags never need clearing between launches (only once,
+    // before their first use, so that stale memory cannot hold a future epoch).
+    float* row_mu = nullptr;              // [M] out (LN fold)
+    float* row_rstd = nullptr;            // [M] out (LN fold)
+    const int32_t* tile_rec = nullptr;    // [n_mtiles] record of each 128-row tile (LN fold)
+    const int32_t* rec_row_off = nullptr; // [records] first row of each record (LN fold)
+    const int32_t* rec_len = nullptr;     // [records] real rows of each record (LN fold)
+    uint64_t* row_flags = nullptr;        // [n_mtiles * 32] (LN fold)
+    uint64_t epoch = 0;                   // set by launch_gemm
     const float* col_c = nullptr;         // [N]    (LN fold)
     void* out = nullptr;
     int64_t ldo = 0;
