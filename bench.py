@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum of one full K/V-projection launch of this
 # workload: an ncu capture of the same kernel on the first 2 records, scaled to 8 records
 # (set to None whenever the kernel changes until it is captured again).
-KV_GEMM_TRAFFIC_BYTES = None
+KV_GEMM_TRAFFIC_BYTES = 2.288e9
 
 
 def load_peaks():

@@ -424,9 +424,8 @@ int cached_plan(const clef_config* cfg, const clef_schema* s, const Plan** plan,
 // reports the device-side errors of the latest call.
 int upload_plan(const Plan& p, void* workspace, void* dst, cudaStream_t st, void* row_flags = nullptr,
                 size_t row_flags_bytes = 0) {
-    if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return CLEF_ERR_CUDA;
-    if (row_flags && cudaMemsetAsync(row_flags, 0, row_flags_bytes, st) != cudaSuccess) return CLEF_ERR_CUDA;
-    if (launch_plan_upload(static_cast<int32_t*>(dst), p.blob.data(), p.blob.size(), st) != cudaSuccess)
+    if (launch_plan_upload(static_cast<int32_t*>(dst), p.blob.data(), p.blob.size(), workspace, 256, row_flags,
+                           row_flags ? row_flags_bytes : 0, st) != cudaSuccess)
         return CLEF_ERR_CUDA;
     return CLEF_OK;
 }

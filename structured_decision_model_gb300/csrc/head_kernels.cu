@@ -2,6 +2,8 @@
 // the option / field streams, split-L routing attention and its merge, field
 // aggregation, field self-attention, scorer input assembly, scoring with the
 // per-question softmax, and the weight-preparation kernels.
+#include <algorithm>
+
 #include "common.cuh"
 #include "head_kernels.h"
 #include "kernels.h"
@@ -640,13 +642,20 @@ static_assert(sizeof(PlanChunk) + sizeof(int32_t*) <= 32764, "kernel parameters 
 
 // One 16-byte unit per thread over several CTAs (reads of the parameter block by
 // different lanes do not broadcast, so the copy is spread out); dst is 16-byte aligned.
-__global__ void __launch_bounds__(256) plan_upload_kernel(int32_t* __restrict__ dst, const __grid_constant__ PlanChunk c) {
+// The launch also clears up to two 16-byte-aligned regions (z0: n0 units, z1: n1 units).
+__global__ void __launch_bounds__(256) plan_upload_kernel(int32_t* __restrict__ dst, const __grid_constant__ PlanChunk c,
+                                                         int4* __restrict__ z0, int n0, int4* __restrict__ z1,
+                                                         int n1) {
     griddep_wait();
     griddep_launch();
     const int i = int(blockIdx.x * blockDim.x + threadIdx.x);
     const int n4 = c.n >> 2;
     if (i < n4) reinterpret_cast<int4*>(dst)[i] = reinterpret_cast<const int4*>(c.data)[i];
     if (i < (c.n & 3)) dst[4 * n4 + i] = c.data[4 * n4 + i];
+    for (int k = i; k < n0 + n1; k += int(gridDim.x * blockDim.x)) {
+        if (k < n0) z0[k] = make_int4(0, 0, 0, 0);
+        else z1[k - n0] = make_int4(0, 0, 0, 0);
+    }
 }
 
 // dst[r][col_off + c] = src[r][c] for a [rows][cols] bf16 block (16-byte units).
@@ -733,14 +742,22 @@ cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s) {
     return launch_pdl(score_softmax_kernel, dim3(Q), dim3(256), smem, s, a);
 }
 
-cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaStream_t s) {
+cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, void* z0, size_t z0_bytes, void* z1,
+                               size_t z1_bytes, cudaStream_t s) {
+    if ((z0_bytes | z1_bytes) % 16 || (reinterpret_cast<uintptr_t>(z0) | reinterpret_cast<uintptr_t>(z1)) % 16 ||
+        z0_bytes / 16 + z1_bytes / 16 >= (size_t(1) << 30))
+        return cudaErrorInvalidValue;
     PlanChunk c;
+    int n0 = int(z0_bytes / 16), n1 = int(z1_bytes / 16);  // cleared by the first chunk's launch
     for (size_t off = 0; off < n; off += kPlanChunkInts) {
         c.n = int32_t(n - off < size_t(kPlanChunkInts) ? n - off : size_t(kPlanChunkInts));
         for (int i = 0; i < c.n; ++i) c.data[i] = src[off + i];
-        const unsigned grid = unsigned((c.n + 1023) / 1024);
-        const cudaError_t e = launch_pdl(plan_upload_kernel, dim3(grid), dim3(256), 0, s, dst + off, c);
+        const int units = std::max((c.n + 3) / 4, std::min(n0 + n1, 64 * 1024));
+        const unsigned grid = unsigned((units + 255) / 256);
+        const cudaError_t e = launch_pdl(plan_upload_kernel, dim3(grid), dim3(256), 0, s, dst + off, c,
+                                         static_cast<int4*>(z0), n0, static_cast<int4*>(z1), n1);
         if (e != cudaSuccess) return e;
+        n0 = n1 = 0;
     }
     return cudaSuccess;
 }

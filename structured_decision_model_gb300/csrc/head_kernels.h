@@ -161,7 +161,10 @@ cudaError_t launch_field_attn(const uint16_t* qkv, int D, int heads, const int32
                               uint16_t* out, cudaStream_t s);
 cudaError_t launch_score_softmax(const ScoreArgs& a, int Q, cudaStream_t s);
 cudaError_t launch_fold_kv(const FoldArgs& a, int rows, cudaStream_t s);
-cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, cudaStream_t s);
+// Copies the plan (n int32 values) to dst and clears z0 / z1 (16-byte aligned, sizes
+// multiples of 16 bytes; null with size 0 when unused).
+cudaError_t launch_plan_upload(int32_t* dst, const int32_t* src, size_t n, void* z0, size_t z0_bytes, void* z1,
+                               size_t z1_bytes, cudaStream_t s);
 cudaError_t launch_copy_cols(uint16_t* dst, int64_t ld_dst, int col_off, const uint16_t* src, int64_t ld_src,
                              int rows, int cols, cudaStream_t s);
 
