@@ -247,12 +247,15 @@ CLEF_API int clef_stream_finish_f16(const clef_config* cfg, const void* const* w
 CLEF_API int clef_device_status(void* workspace, void* stream);
 
 /* Self-test of the device-side wait limits (the pages have no counterpart: this is a
- * property of this implementation).  Clears the status word of `workspace` (device
+ * property of this implementation).  Clears the first 256 bytes of `workspace` (device
  * memory, 256-byte aligned, at least 256 bytes) and launches one kernel whose single
- * waiting thread waits on a barrier that never completes, for `limit_ns` nanoseconds
- * (1 us .. 100 ms).  The wait gives up, sets the timeout bit and the kernel returns:
- * clef_device_status then reports CLEF_ERR_DEVICE_TIMEOUT and the CUDA context stays
- * usable.  Every wait of the head's own kernels has the same form, with a 2 s limit.
+ * waiting thread waits, for `limit_ns` nanoseconds (1 us .. 100 ms) each, first on a
+ * shared-memory barrier that never completes, then on a global flag (at byte 128 of
+ * the workspace) that nothing sets.  Each wait gives up, sets the timeout bit and
+ * records itself in the int32 at byte 8 of the workspace (bit 0: the barrier wait,
+ * bit 1: the flag wait); the kernel returns.  clef_device_status then reports
+ * CLEF_ERR_DEVICE_TIMEOUT and the CUDA context stays usable.  Every wait of the head's
+ * own kernels has one of these two forms, with a 2 s limit.
  * Returns CLEF_ERR_INVALID_ARGUMENT for a null or misaligned workspace or a limit out
  * of range, CLEF_ERR_CUDA if the launch fails, else CLEF_OK (asynchronously). */
 CLEF_API int clef_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* stream);

@@ -311,28 +311,36 @@ __global__ void __launch_bounds__(256) route_attn_merge_kernel(const RouteAttnAr
     const int nch = (a.lengths[b] + kAttnChunk - 1) / kAttnChunk;
     const int64_t p0 = a.rec_part_off[b] + int64_t(h) * O_b + (o - o_base);  // chunk k at p0 + k * heads * O_b
     const int64_t pstride = int64_t(a.heads) * O_b;
-    // lane k holds chunk k's statistics (32 chunks at a time): one round trip for all of them
-    float M = -INFINITY;
-    for (int k = lane; k < nch; k += 32) M = fmaxf(M, a.pm[p0 + k * pstride]);
-    M = warp_max(M);
-    float Ls = 0.f, x0 = 0.f, x1 = 0.f;
-    for (int k0 = 0; k0 < nch; k0 += 32) {
-        const int k = k0 + lane;
-        float w = 0.f;
-        if (k < nch) {
-            w = exp2f(a.pm[p0 + k * pstride] - M);
-            Ls += a.pl[p0 + k * pstride] * w;
+    // Chunks in groups of 8: every load of a group (lane k: chunk k's maximum and sum;
+    // all lanes: two dims of each chunk's accumulator) is issued before any is used, so
+    // a group costs one round trip; groups after the first rescale what came before.
+    float M = -INFINITY, Ls = 0.f, x0 = 0.f, x1 = 0.f;
+    for (int k0 = 0; k0 < nch; k0 += 8) {
+        const int nk = min(8, nch - k0);
+        float pmk = -INFINITY, plk = 0.f;
+        if (lane < nk) {
+            pmk = a.pm[p0 + (k0 + lane) * pstride];
+            plk = a.pl[p0 + (k0 + lane) * pstride];
         }
-        const int nk = min(32, nch - k0);
-#pragma unroll 8
-        for (int j = 0; j < nk; ++j) {  // chunks in order; the weights come from their lanes
+        float2 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = j < nk ? *reinterpret_cast<const float2*>(a.pacc + (p0 + (k0 + j) * pstride) * 64 + lane * 2)
+                          : make_float2(0.f, 0.f);
+        const float nm = fmaxf(M, warp_max(pmk));
+        const float corr = exp2f(M - nm);  // 0 for the first group
+        const float w = lane < nk ? exp2f(pmk - nm) : 0.f;
+        Ls = Ls * corr + warp_sum(plk * w);
+        x0 *= corr;
+        x1 *= corr;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // chunks in order; the weights come from their lanes
             const float wj = __shfl_sync(0xffffffffu, w, j);
-            const float2 v = *reinterpret_cast<const float2*>(a.pacc + (p0 + (k0 + j) * pstride) * 64 + lane * 2);
-            x0 += v.x * wj;
-            x1 += v.y * wj;
+            x0 += v[j].x * wj;
+            x1 += v[j].y * wj;
         }
+        M = nm;
     }
-    Ls = warp_sum(Ls);
     const float inv = 1.0f / Ls;
     *reinterpret_cast<uint32_t*>(a.out + int64_t(o) * a.ldo + h * 64 + lane * 2) = pack_bf16(x0 * inv, x1 * inv);
 }

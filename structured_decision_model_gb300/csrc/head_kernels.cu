@@ -672,15 +672,21 @@ __global__ void __launch_bounds__(256) copy_cols_kernel(uint16_t* __restrict__ d
 
 // =====================================================================
 // Self-test of the bounded waits: one thread waits on an mbarrier that nothing ever
-// completes, with a short limit, so the wait runs out, sets the timeout bit of the
-// status word and returns.  No thread hangs and nothing faults.
+// completes, then on a global flag that nothing sets, each with a short limit, so each
+// wait runs out, sets the timeout bit of the status word and returns; flags[2] records
+// which waits gave up (bit 0: barrier, bit 1: flag).  No thread hangs and nothing faults.
 // =====================================================================
 __global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(int* flags, uint64_t limit_ns) {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         fence_barrier_init();
-        mbar_wait_bounded(&bar, 0, nullptr, flags, limit_ns);  // phase 0 never completes
+        int gave_up = 0;
+        if (!mbar_wait_bounded(&bar, 0, nullptr, flags, limit_ns)) gave_up |= 1;  // phase 0 never completes
+        // the flag at byte 128 of the cleared block stays 0; the wait is for 1
+        if (!flag_wait_bounded(reinterpret_cast<const uint64_t*>(flags + 32), 1, nullptr, flags, limit_ns))
+            gave_up |= 2;
+        flags[2] = gave_up;
     }
     __syncwarp();
 }
