@@ -30,9 +30,9 @@
 // CTA of the launch and paced by its producer, read from L2 just ahead of the GEMM's own
 // copies of the rows (shared memory has no bandwidth to spare next to the MMAs), each
 // warp publishing its 4 rows through a flag that the epilogues of every tile of those
-// rows wait for before applying the fold.  The rows are read from HBM once.
-// Every mbarrier wait is bounded: on a timeout the CTA sets the timeout flag,
-// waits (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
+// rows wait for before applying the fold (warps 6..9).  The rows are read from HBM once.
+// Every wait (mbarrier, flag, pacing) is bounded: on a timeout the CTA sets the timeout
+// flag, waits (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
