@@ -181,7 +181,12 @@ typedef struct clef_debug_outputs {
  *   workspace  device scratch of clef_workspace_size bytes, 256-byte aligned.
  *   debug      optional (NULL) intermediate outputs.
  * Host-side validation errors return before any launch.  The call does not wait
- * for the GPU: device-side bound / timeout flags are read by clef_device_status. */
+ * for the GPU: device-side bound / timeout flags are read by clef_device_status.
+ * Every device step of a call without `debug` is a kernel launch on `stream`, so
+ * after one ordinary call with the same arguments the call can be captured into a
+ * CUDA graph; each replay uploads the captured plan, clears the status word and the
+ * memory statistics' flags, and recomputes the whole head from the buffers' contents
+ * at replay time. */
 CLEF_API int clef_head_forward(const clef_config* cfg, const void* const* weights, const void* prepared,
                       const clef_schema* schema, const uint16_t* hidden, const int32_t* token_ids,
                       const uint16_t* lexical, float* logits, float* probs, float* q_value,
