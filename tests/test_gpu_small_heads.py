@@ -30,6 +30,9 @@ SHAPES = [
     synth.HeadShape(H=192, D=64, heads=1, F=128, n_route=1, n_joint=1, vocab=3000),
     synth.HeadShape(H=320, D=128, heads=2, F=192, n_route=2, n_joint=2, vocab=3000),
 ]
+# one 128-wide column tile per row tile and more row tiles (157) than CTAs: each CTA
+# walks two tiles and the statistics jobs of a tile belong to other CTAs
+NARROW = synth.HeadShape(H=64, D=64, heads=1, F=64, n_route=1, n_joint=1, vocab=3000)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,8 +41,8 @@ def _lib():
     B.load()
 
 
-def _batch(shape, seed):
-    spec = synth.BatchSpec(name="small", B=4, H=shape.H, vocab=shape.vocab, lengths=[130, 127, 129, 300],
+def _batch(shape, seed, lengths=(130, 127, 129, 300)):
+    spec = synth.BatchSpec(name="small", B=len(lengths), H=shape.H, vocab=shape.vocab, lengths=list(lengths),
                            questions=(2, 3), options=(2, 4), instr_len=(4, 12), option_len=(2, 8))
     bt = synth.make_batch(spec, seed=seed)
     rng = np.random.default_rng(seed)
@@ -74,6 +77,17 @@ def test_small_head_forward_and_stream(shape):
     inputs = device_inputs(bt, shape.vocab)
     gpu = run_gpu(head, bt, inputs=inputs)
     compare(gpu, run_oracle(w, shape, bt), bt)
+    streamed = _stream(head, bt, inputs)
+    for k in gpu:
+        np.testing.assert_array_equal(streamed[k], gpu[k])
+
+
+def test_narrow_head_long_records_one_column_tile():
+    bt = _batch(NARROW, seed=47, lengths=(9000, 11000))
+    head, w = head_for(NARROW)
+    inputs = device_inputs(bt, NARROW.vocab)
+    gpu = run_gpu(head, bt, inputs=inputs)
+    compare(gpu, run_oracle(w, NARROW, bt), bt)
     streamed = _stream(head, bt, inputs)
     for k in gpu:
         np.testing.assert_array_equal(streamed[k], gpu[k])
