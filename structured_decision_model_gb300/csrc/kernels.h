@@ -53,10 +53,10 @@ struct GemmEpilogue {
     // LN fold: the row statistics are written to row_mu / row_rstd for rows m < M.  With
     // tile_rec given, row m belongs to record b = tile_rec[m / 128] and is a padding row
     // when m - rec_row_off[b] >= rec_len[b] (without: every row m < M is real); padding
-    // rows get mu = rstd = 0 and are stored as zeros.  row_flags[m / 4] (n_mtiles * 32 entries)
-    // is set to `epoch` once rows m .. m + 3 are published; the launcher assigns each
-    // launch a new epoch, so the flags never need clearing between launches (only once,
-    // before their first use, so that stale memory cannot hold a future epoch).
+    // rows get mu = rstd = 0 and are stored as zeros.  row_flags[g] (n_mtiles * 32 entries)
+    // is set to `epoch` once rows 4g .. 4g + 3 are published.  The launcher gives each
+    // launch a new epoch, so flags left by earlier launches never match; the caller clears
+    // the flags beforehand so that no other earlier content can match either.
     float* row_mu = nullptr;              // [M] out (LN fold)
     float* row_rstd = nullptr;            // [M] out (LN fold)
     const int32_t* tile_rec = nullptr;    // [n_mtiles] record of each 128-row tile (LN fold)
