@@ -161,6 +161,13 @@ typedef struct clef_debug_outputs {
      * where the head shape allows it (width 1024, 16 heads, FFN 4096, at most 256
      * options per record).  The outputs agree within the parity tolerance either way. */
     int32_t tail_mode;
+    /* Optional fp32 [R] each (NULL = not written): the memory LayerNorm statistics of
+     * every compact row as the K/V projection computed them (mean, 1/sqrt(var + 1e-5)).
+     * Record b's row t < lengths[b] is compact row R_b + t, R_b = the sum over b' < b of
+     * lengths[b'] rounded up to a multiple of 128, and R = that sum over every record;
+     * the round-up rows hold 0. */
+    float* row_mu;
+    float* row_rstd;
 } clef_debug_outputs;
 
 /* The forward pass.

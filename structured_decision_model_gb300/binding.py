@@ -48,7 +48,8 @@ class ClefSchema(ctypes.Structure):
 class ClefDebugOutputs(ctypes.Structure):
     _fields_ = [("pooled_u", _vp), ("pooled_c", _vp), ("pooled_x", _vp), ("global_g", _vp),
                 ("option_final", _vp), ("field_final", _vp), ("events", _vp * 8), ("timeline", _vp),
-                ("timeline_len", _i32), ("timeline_count", _vp), ("tail_mode", _i32)]
+                ("timeline_len", _i32), ("timeline_count", _vp), ("tail_mode", _i32), ("row_mu", _vp),
+                ("row_rstd", _vp)]
 
 
 _lib = None

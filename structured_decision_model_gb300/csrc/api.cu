@@ -606,8 +606,11 @@ bool use_record_tail(const clef_config* c, const Plan& p, const clef_debug_outpu
 
 // Debug copies and the launch count, after the last kernel of the forward pass.
 int finish_debug(const clef_debug_outputs* debug, int n_launch, int Q, int O, int B, int H, int D, const float* u32,
-                 const float* x32, const float* g32, const float* o_hat, const float* f_hat, cudaStream_t st) {
+                 const float* x32, const float* g32, const float* o_hat, const float* f_hat, const float* mu,
+                 const float* rstd, int R, cudaStream_t st) {
     if (!debug) return CLEF_OK;
+    if (debug->row_mu) CK(cudaMemcpyAsync(debug->row_mu, mu, size_t(R) * 4, cudaMemcpyDeviceToDevice, st));
+    if (debug->row_rstd) CK(cudaMemcpyAsync(debug->row_rstd, rstd, size_t(R) * 4, cudaMemcpyDeviceToDevice, st));
     if (debug->timeline_count) CK(cudaMemcpyAsync(debug->timeline_count, &n_launch, 4, cudaMemcpyHostToDevice, st));
     if (debug->pooled_u) CK(cudaMemcpyAsync(debug->pooled_u, u32, size_t(Q) * H * 4, cudaMemcpyDeviceToDevice, st));
     if (debug->pooled_x) CK(cudaMemcpyAsync(debug->pooled_x, x32, size_t(O) * H * 4, cudaMemcpyDeviceToDevice, st));
@@ -808,7 +811,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
         rt.o_hat = o_hat; rt.f_hat = f_hat; rt.ln_buf = ln_buf; rt.attn_buf = attn_buf; rt.hid_buf = hid_buf; rt.z = z;
         rt.logits = logits; rt.probs = probs; rt.q_value = q_value; rt.q_conf = q_conf; rt.q_argmax = q_argmax;
         CK(launch_record_tail(rt, st)); CK(tick());
-        return finish_debug(debug, n_launch, Q, O, B, H, D, u32, x32, g32, o_hat, f_hat, st);
+        return finish_debug(debug, n_launch, Q, O, B, H, D, u32, x32, g32, o_hat, f_hat, mu, rstd, p.R, st);
     }
     // 6. fields: [u | g | summary] [W_fu | W_fg | W_fs]^T + b + type embedding (bias and
     // type-embedding row added with the partial products by the first joint LayerNorm)
@@ -861,7 +864,7 @@ int forward_impl(const clef_config* cfg, const void* const* weights, const void*
     sc.joint_scale = W(weights, wi.tail(3));
     sc.logits = logits; sc.probs = probs; sc.q_value = q_value; sc.q_conf = q_conf; sc.q_argmax = q_argmax;
     CK(launch_score_softmax(sc, Q, st)); CK(tick());
-    return finish_debug(debug, n_launch, Q, O, B, H, D, u32, x32, g32, o_hat, f_hat, st);
+    return finish_debug(debug, n_launch, Q, O, B, H, D, u32, x32, g32, o_hat, f_hat, mu, rstd, p.R, st);
 }
 
 // Statistics and K/V of rows [row0, row0 + n_rows) of one record.  fp16 rows are first

@@ -182,6 +182,58 @@ def test_ln_fold_rows_with_offsets_and_outlier_channels():
     print("lnfold", compare(gpu, ref, bt))
 
 
+def test_memory_statistics_against_fp64():
+    """The memory LayerNorm statistics as the K/V projection computes them (shifted fp32
+    sums over each hidden row, "clef-flash-CoreAI metadata.json" decision.head.reads: the
+    head normalises the final-norm states), against the fp64 mean and biased variance of
+    the same bf16 rows, on rows with per-row offsets up to 40 and outlier channels x50;
+    the round-up rows of every record hold 0.  Then streamed in 64-row chunks, the same
+    statistics bit for bit."""
+    spec = synth.BatchSpec(name="stats", B=3, lengths=[300, 1029, 2048], questions=(2, 4), options=(2, 5))
+    bt = synth.make_batch(spec, seed=23)
+    rng = np.random.default_rng(23)
+    h = synth.bf16_to_f32(bt.hidden)
+    h += rng.uniform(-40, 40, size=(bt.B, bt.Lpad, 1)).astype(np.float32)
+    ch = rng.choice(bt.H, size=6, replace=False)
+    h[:, :, ch] *= 50.0
+    bt = dataclasses.replace(bt, hidden=synth.f32_to_bf16(h))
+    head, _ = head_for(FULL)
+    rows = [(int(l) + 127) // 128 * 128 for l in bt.lengths]
+    R = sum(rows)
+    def stats_of(run):
+        mu = torch.full((R,), 7.0, dtype=torch.float32, device="cuda")
+        rs = torch.full((R,), 7.0, dtype=torch.float32, device="cuda")
+        dbg = B.ClefDebugOutputs()
+        dbg.row_mu, dbg.row_rstd = mu.data_ptr(), rs.data_ptr()
+        run(dbg)
+        torch.cuda.synchronize()
+        return mu.cpu().numpy(), rs.cpu().numpy()
+    inputs = device_inputs(bt, FULL.vocab)
+    mu, rs = stats_of(lambda dbg: run_gpu(head, bt, debug=dbg, inputs=inputs))
+    x = synth.bf16_to_f32(bt.hidden).astype(np.float64)
+    off = 0
+    for b in range(bt.B):
+        L = int(bt.lengths[b])
+        ref_mu = x[b, :L].mean(axis=1)
+        ref_rs = 1.0 / np.sqrt(x[b, :L].var(axis=1) + 1e-5)
+        np.testing.assert_allclose(mu[off:off + L], ref_mu, rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(rs[off:off + L], ref_rs, rtol=1e-4)
+        assert not mu[off + L:off + rows[b]].any() and not rs[off + L:off + rows[b]].any()
+        off += rows[b]
+
+    def streamed(dbg):
+        hidden, ids, lex = inputs
+        sch = schema_of(bt)
+        head.stream_begin(sch)
+        for b in range(bt.B):
+            for r0 in range(0, int(bt.lengths[b]), 64):
+                head.stream_rows(sch, hidden, b, r0, min(64, int(bt.lengths[b]) - r0))
+        head.stream_finish(sch, hidden, ids, lex, debug=dbg)
+    smu, srs = stats_of(streamed)
+    np.testing.assert_array_equal(smu, mu)
+    np.testing.assert_array_equal(srs, rs)
+
+
 def ragged_spec(**kw):
     d = dict(name="ragged", B=3, length_law="uniform", length_range=(700, 2600), questions=(3, 6),
              options=(2, 7))
